@@ -192,35 +192,53 @@ void orc_dequant(const uint8_t* q, const uint16_t* scales, const int32_t* zeros,
 /* GEMM in float64:  C[m][n] = sum_k A[m][k] * W[n][k]                          */
 /* ------------------------------------------------------------------------- */
 
-static double dot_row(const uint16_t* a, const uint16_t* w, int64_t K, int dtype) {
+static double dot_values(const double* a, const double* w, int64_t K) {
     double acc = 0.0;
-    for (int64_t k = 0; k < K; ++k) acc += dt_value(a[k], dtype) * dt_value(w[k], dtype);
+    for (int64_t k = 0; k < K; ++k) acc += a[k] * w[k];
     return acc;
+}
+
+/* Selected rows of C: out[i][n] = C[rows[i]][n] = sum_k A[rows[i]][k] W[n][k].
+ * Each operand row is decoded to exact float64 values once; the sum runs over
+ * k in increasing order. */
+void orc_gemm_rows(const uint16_t* A, const uint16_t* W, const int64_t* rows, int64_t nrows,
+                   int64_t N, int64_t K, int dtype, double* out) {
+    double* a = (double*)malloc((size_t)(nrows * K) * sizeof(double));
+    if (!a) return;
+    for (int64_t i = 0; i < nrows; ++i)
+        for (int64_t k = 0; k < K; ++k) a[i * K + k] = dt_value(A[rows[i] * K + k], dtype);
+#pragma omp parallel
+    {
+        double* w = (double*)malloc((size_t)K * sizeof(double));
+#pragma omp for schedule(static)
+        for (int64_t n = 0; n < N; ++n) {
+            for (int64_t k = 0; k < K; ++k) w[k] = dt_value(W[n * K + k], dtype);
+            for (int64_t i = 0; i < nrows; ++i) out[i * N + n] = dot_values(a + i * K, w, K);
+        }
+        free(w);
+    }
+    free(a);
 }
 
 void orc_gemm(const uint16_t* A, const uint16_t* W, int64_t M, int64_t N, int64_t K,
               int dtype, double* C) {
-#pragma omp parallel for collapse(2) schedule(static)
-    for (int64_t m = 0; m < M; ++m)
-        for (int64_t n = 0; n < N; ++n)
-            C[m * N + n] = dot_row(A + m * K, W + n * K, K, dtype);
-}
-
-/* Selected rows of C: out[i][n] = C[rows[i]][n]. */
-void orc_gemm_rows(const uint16_t* A, const uint16_t* W, const int64_t* rows, int64_t nrows,
-                   int64_t N, int64_t K, int dtype, double* out) {
-#pragma omp parallel for collapse(2) schedule(static)
-    for (int64_t i = 0; i < nrows; ++i)
-        for (int64_t n = 0; n < N; ++n)
-            out[i * N + n] = dot_row(A + rows[i] * K, W + n * K, K, dtype);
+    int64_t* rows = (int64_t*)malloc((size_t)(M > 0 ? M : 1) * sizeof(int64_t));
+    if (!rows) return;
+    for (int64_t m = 0; m < M; ++m) rows[m] = m;
+    orc_gemm_rows(A, W, rows, M, N, K, dtype, C);
+    free(rows);
 }
 
 /* Selected elements: out[i] = C[ms[i]][ns[i]]. */
 void orc_gemm_pairs(const uint16_t* A, const uint16_t* W, const int64_t* ms, const int64_t* ns,
                     int64_t npairs, int64_t K, int dtype, double* out) {
 #pragma omp parallel for schedule(static)
-    for (int64_t i = 0; i < npairs; ++i)
-        out[i] = dot_row(A + ms[i] * K, W + ns[i] * K, K, dtype);
+    for (int64_t i = 0; i < npairs; ++i) {
+        double acc = 0.0;
+        for (int64_t k = 0; k < K; ++k)
+            acc += dt_value(A[ms[i] * K + k], dtype) * dt_value(W[ns[i] * K + k], dtype);
+        out[i] = acc;
+    }
 }
 
 /* The whole layer in the pages' order on a packed weight: unpack -> dequant ->

@@ -1,0 +1,119 @@
+"""Host-side checks of the C ABI: the library loads, exports every symbol the
+header declares, and validates arguments before touching the GPU."""
+
+import os
+import re
+
+import pytest
+
+from w4a16_int4_weight_gb300 import build as wbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def B():
+    wbuild.build()
+    from w4a16_int4_weight_gb300 import binding
+    return binding
+
+
+def header_symbols():
+    with open(os.path.join(ROOT, "include", "w4a16.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:[\w\s\*]+?)\b(w4a16_\w+)\s*\(", text, re.M)))
+
+
+def test_library_exports_every_declared_symbol(B):
+    syms = header_symbols()
+    assert len(syms) >= 10
+    for s in syms:
+        assert hasattr(B.lib, s), s
+    assert set(syms) == set(B.EXPORTED)
+    assert B.version() == 100
+
+
+def test_packed_layout_sizes(B):
+    # K=4096: K/8 = 512 words (already a multiple of 4); scales N x 32 bf16
+    tot, so, zo, ldq = B.packed_layout(4096, 4096, 128, "uint4b8", "bf16")
+    assert ldq == 512 and so == 4096 * 512 * 4 and zo == 0
+    assert tot == so + 4096 * 32 * 2
+    # K=48: K/8 = 6 words -> pitch 8; sections on 256-byte boundaries
+    tot, so, zo, ldq = B.packed_layout(8, 48, -1, "uint4", "fp16")
+    assert ldq == 8 and so == 256 and zo == 512 and tot == 768
+    tot, so, zo, ldq = B.packed_layout(11008, 4096, 32, "uint4", "bf16")
+    assert so == 11008 * 512 * 4
+    assert zo == so + 11008 * 128 * 2
+    assert tot == zo + (11008 // 8) * 128 * 4
+
+
+FAKE = 1 << 20   # any 256-aligned address: validation rejects before it is used
+
+
+@pytest.mark.parametrize("args,needle", [
+    (dict(K=24), "divisible by 16"),
+    (dict(K=0), "out of range"),
+    (dict(N=0), "out of range"),
+    (dict(G=96), "group size"),
+    (dict(K=4096 + 16, G=128), "divisible by group_size"),
+    (dict(qtype=7), "quant type"),
+    (dict(dtype=5), "dtype"),
+    (dict(qtype=1, N=12), "divisible by 8"),
+    (dict(qtype=1, zeros=0), "zeros"),
+    (dict(qtype=0, zeros=FAKE), "NULL for uint4b8"),
+    (dict(A=FAKE + 2), "A must be"),
+    (dict(Wq=FAKE + 4), "Wq must be"),
+    (dict(scales=0), "scales must be"),
+    (dict(C=0), "C must be"),
+    (dict(M=-1), "M=-1"),
+    (dict(path=9), "unknown path"),
+    (dict(path=3), "dense copy"),
+    (dict(path=1, M=65), "M <= 64"),
+])
+def test_gemm_rejects_invalid_arguments(B, args, needle):
+    a = dict(A=FAKE, Wq=FAKE, scales=FAKE, zeros=None, Wdense=None, C=FAKE, M=4, N=256, K=4096,
+             G=128, qtype=0, dtype=1, path=0)
+    a.update(args)
+    if a["qtype"] == 1 and "zeros" not in args:
+        a["zeros"] = FAKE
+    code = B.lib.w4a16_gemm_ex(a["A"], a["Wq"], a["scales"], a["zeros"], a["Wdense"], a["C"],
+                               a["M"], a["N"], a["K"], a["G"], a["qtype"], a["dtype"], a["path"], None)
+    assert code == B.ERR_INVALID_ARG
+    assert needle in B.last_error()
+
+
+def test_m_zero_is_a_noop(B):
+    assert B.lib.w4a16_gemm(FAKE, FAKE, FAKE, None, FAKE, 0, 256, 4096, 128, 0, 1, None) == B.OK
+
+
+def test_pack_and_dequant_validation(B):
+    assert B.lib.w4a16_pack(FAKE + 1, FAKE, None, FAKE, 64, 64, 32, 0, 0, None) == B.ERR_INVALID_ARG
+    assert "q must be" in B.last_error()
+    assert B.lib.w4a16_pack(FAKE, FAKE, None, FAKE + 16, 64, 64, 32, 0, 0, None) == B.ERR_INVALID_ARG
+    assert "Wpacked" in B.last_error()
+    assert B.lib.w4a16_dequant(FAKE, FAKE, None, FAKE + 8, 64, 64, 32, 0, 0, None) == B.ERR_INVALID_ARG
+    assert "W must be" in B.last_error()
+    assert B.lib.w4a16_gemm_dense(FAKE, FAKE, FAKE, 4, 64, 40, 1, None) == B.ERR_INVALID_ARG
+    assert "multiple of 16" in B.last_error()
+
+
+def test_router(B):
+    # small M -> decode; large M -> fused; dense copy used only for large M
+    assert B.route(1, 4096, 4096, 128, "uint4b8", "bf16") == B.PATH_DECODE
+    assert B.route(16, 11008, 4096, 32, "uint4", "bf16") == B.PATH_DECODE
+    assert B.route(2048, 14336, 4096, 128, "uint4b8", "bf16") == B.PATH_FUSED
+    assert B.route(2048, 14336, 4096, 128, "uint4b8", "bf16", has_dense=True) == B.PATH_DENSE
+    assert B.route(4, 14336, 4096, 128, "uint4b8", "bf16", has_dense=True) == B.PATH_DECODE
+    assert B.route(4, 14336, 4100, 128, "uint4b8", "bf16") == -1
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    import importlib.util
+    src = os.path.join(ROOT, "w4a16_int4_weight_gb300", "binding.py")
+    # load a copy of the binding from a directory with no library next to it
+    dst = tmp_path / "binding.py"
+    dst.write_text(open(src).read())
+    spec = importlib.util.spec_from_file_location("binding_copy", dst)
+    mod = importlib.util.module_from_spec(spec)
+    with pytest.raises(ImportError, match="not built"):
+        spec.loader.exec_module(mod)

@@ -1,0 +1,157 @@
+"""Thin ctypes binding of libw4a16 (C ABI in include/w4a16.h).
+
+Argument marshalling only: every entry point forwards raw device pointers,
+sizes and the current CUDA stream to the library, which validates and runs all
+of the work in its own kernels.  Importing this module fails loudly if the
+library has not been built (``python -m w4a16_int4_weight_gb300.build``);
+there is no fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libw4a16.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE_TIMEOUT = range(5)
+UINT4B8, UINT4 = 0, 1
+FP16, BF16 = 0, 1
+PATH_AUTO, PATH_DECODE, PATH_FUSED, PATH_DENSE = range(4)
+QTYPES = {"uint4b8": UINT4B8, "uint4": UINT4}
+DTYPES = {"fp16": FP16, "bf16": BF16}
+PATHS = {"auto": PATH_AUTO, "decode": PATH_DECODE, "fused": PATH_FUSED, "dense": PATH_DENSE}
+
+
+class W4A16Error(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"w4a16 error {code}: {message}")
+        self.code = code
+
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"libw4a16.so is not built ({LIB_PATH}); run "
+                      "`python -m w4a16_int4_weight_gb300.build`")
+
+lib = ctypes.CDLL(LIB_PATH)
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_I = ctypes.c_int
+_SZ = ctypes.POINTER(ctypes.c_size_t)
+
+_SIGS = {
+    "w4a16_version": (_I, []),
+    "w4a16_last_error_string": (ctypes.c_char_p, []),
+    "w4a16_packed_layout": (_I, [_I64, _I64, _I, _I, _I, _SZ, _SZ, _SZ, ctypes.POINTER(_I64)]),
+    "w4a16_pack": (_I, [_P, _P, _P, _P, _I64, _I64, _I, _I, _I, _P]),
+    "w4a16_gemm": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _P]),
+    "w4a16_gemm_ex": (_I, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _I, _P]),
+    "w4a16_route": (_I, [_I64, _I64, _I64, _I, _I, _I, _I]),
+    "w4a16_dequant": (_I, [_P, _P, _P, _P, _I64, _I64, _I, _I, _I, _P]),
+    "w4a16_gemm_dense": (_I, [_P, _P, _P, _I64, _I64, _I64, _I, _P]),
+    "w4a16_device_status": (_I, [ctypes.POINTER(_I)]),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _f = getattr(lib, _name)
+    _f.restype = _res
+    _f.argtypes = _args
+
+EXPORTED = tuple(_SIGS)
+
+
+def last_error() -> str:
+    return lib.w4a16_last_error_string().decode()
+
+
+def _check(code: int) -> None:
+    if code != OK:
+        raise W4A16Error(code, last_error())
+
+
+def _ptr(x):
+    """Device/host address of a torch tensor, an int address, or None."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _qt(qtype):
+    return QTYPES[qtype] if isinstance(qtype, str) else int(qtype)
+
+
+def _dt(dtype):
+    if isinstance(dtype, str):
+        return DTYPES[dtype]
+    try:
+        import torch
+        if dtype is torch.float16:
+            return FP16
+        if dtype is torch.bfloat16:
+            return BF16
+    except ImportError:
+        pass
+    return int(dtype)
+
+
+def version() -> int:
+    return lib.w4a16_version()
+
+
+def packed_layout(N, K, G, qtype, dtype):
+    """(total_bytes, scales_off, zeros_off, ldq_words) of the packed buffer."""
+    tot, so, zo = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    ldq = ctypes.c_int64()
+    _check(lib.w4a16_packed_layout(N, K, G, _qt(qtype), _dt(dtype), ctypes.byref(tot),
+                                   ctypes.byref(so), ctypes.byref(zo), ctypes.byref(ldq)))
+    return tot.value, so.value, zo.value, ldq.value
+
+
+def pack(q, scales, zeros, Wpacked, N, K, G, qtype, dtype, stream=None):
+    _check(lib.w4a16_pack(_ptr(q), _ptr(scales), _ptr(zeros), _ptr(Wpacked), N, K, G,
+                          _qt(qtype), _dt(dtype), _stream(stream)))
+
+
+def gemm(A, Wq, scales, zeros, C, M, N, K, G, qtype, dtype, stream=None):
+    _check(lib.w4a16_gemm(_ptr(A), _ptr(Wq), _ptr(scales), _ptr(zeros), _ptr(C), M, N, K, G,
+                          _qt(qtype), _dt(dtype), _stream(stream)))
+
+
+def gemm_ex(A, Wq, scales, zeros, Wdense, C, M, N, K, G, qtype, dtype, path="auto",
+            stream=None):
+    p = PATHS[path] if isinstance(path, str) else int(path)
+    _check(lib.w4a16_gemm_ex(_ptr(A), _ptr(Wq), _ptr(scales), _ptr(zeros), _ptr(Wdense),
+                             _ptr(C), M, N, K, G, _qt(qtype), _dt(dtype), p, _stream(stream)))
+
+
+def route(M, N, K, G, qtype, dtype, has_dense=False) -> int:
+    return lib.w4a16_route(M, N, K, G, _qt(qtype), _dt(dtype), int(bool(has_dense)))
+
+
+def dequant(Wq, scales, zeros, W, N, K, G, qtype, dtype, stream=None):
+    _check(lib.w4a16_dequant(_ptr(Wq), _ptr(scales), _ptr(zeros), _ptr(W), N, K, G,
+                             _qt(qtype), _dt(dtype), _stream(stream)))
+
+
+def gemm_dense(A, W, C, M, N, K, dtype, stream=None):
+    _check(lib.w4a16_gemm_dense(_ptr(A), _ptr(W), _ptr(C), M, N, K, _dt(dtype),
+                                _stream(stream)))
+
+
+def device_status():
+    """(status code, wait site) after synchronising the device; clears the status."""
+    site = ctypes.c_int(0)
+    code = lib.w4a16_device_status(ctypes.byref(site))
+    return code, site.value

@@ -1,0 +1,271 @@
+// Large-M ("prefill") W4A16 GEMM on the 5th-generation tensor cores.
+//
+// The pages' prefill kernel (_triton_w4a16_skinny_fmt_kernel, both revisions)
+// loads a packed weight tile per K step, unpacks it, forms (q - z).to(dtype) *
+// scale and feeds a dot product with fp32 accumulation.  Here the same tile
+// algebra runs as a warp-specialised tcgen05 pipeline:
+//
+//   warp 4     TMA producer: per 64-wide K block, the activation tile
+//              [BT tokens x 64] (128-byte swizzle) and either the packed weight
+//              tile [128 rows x 8 words] (fused) or the dense weight tile
+//              [128 x 64] (dense path), into a 4-stage ring.
+//   warps 0-3  dequantisers (fused path): thread i owns weight row i of the
+//              tile, unpacks 64 K-values with LOP3 magic-number unpacks, forms
+//              rne((q - z) * s) exactly as the pages do, and stores the bf16/fp16
+//              tile in the 128-byte-swizzled K-major layout the tensor core
+//              reads.  After the K loop the same warps are the epilogue.
+//   warp 5     allocates TMEM and issues tcgen05.mma (one thread): the weight
+//              tile is the MMA's A operand (M = 128 weight rows), the activation
+//              tile the B operand (N = BT tokens), fp32 accumulator in TMEM, so
+//              each dequantised weight feeds BT multiply-adds.
+//   epilogue   tcgen05.ld of the accumulator (lane = weight row, column =
+//              token), RNE to the dtype, stores of C[token][row]: the 32 lanes
+//              of a warp write 32 consecutive output columns.
+#include "common.cuh"
+#include "internal.h"
+
+namespace w4a16 {
+namespace {
+
+constexpr int kBM = 128;                  // weight rows per CTA (UMMA M)
+constexpr int kBK = 64;                   // K per stage: one 128-byte swizzle row of 16-bit values
+constexpr int kStages = 4;
+constexpr int kThreads = 192;
+constexpr int kWtBytes = kBM * 128;       // 16 KB dequantised / dense weight tile
+constexpr int kPkBytes = kBM * 32;        // 4 KB packed tile (8 words per row)
+
+__device__ int g_status;
+
+struct Params {
+    const uint16_t* scales;
+    const int32_t* zeros;
+    uint16_t* C;
+    int M, N, K, g_eff, ng;
+    int nkb;   // ceil(K / kBK)
+};
+
+template <int BT, bool DENSE>
+struct Layout {
+    static constexpr int kActBytes = BT * 128;
+    static constexpr int kStageBytes = kActBytes + kWtBytes + (DENSE ? 0 : kPkBytes);
+    static constexpr int kBarOff = kStages * kStageBytes;
+    static constexpr int kBytes = kBarOff + 256 + 1024;   // + barriers, + alignment slack
+};
+
+template <bool BF16, bool ZP, int BT, bool DENSE>
+__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                                                              const __grid_constant__ CUtensorMap tmap_w,
+                                                              const Params p) {
+    using L = Layout<BT, DENSE>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    auto act_tile = [&](int s) { return smem + s * L::kStageBytes; };
+    auto wt_tile = [&](int s) { return smem + s * L::kStageBytes + L::kActBytes; };
+    auto pk_tile = [&](int s) { return smem + s * L::kStageBytes + L::kActBytes + kWtBytes; };
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+    uint64_t* dq_full = full + kStages;
+    uint64_t* empty = dq_full + kStages;
+    uint64_t* acc_full = empty + kStages;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int n0 = blockIdx.x * kBM;
+    const int m0 = blockIdx.y * BT;
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&dq_full[s], 4);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(acc_full, 1);
+        fence_mbar_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(tmem_slot, BT);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_d = *tmem_slot;
+
+    if (warp == 4) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            tma_prefetch_desc(&tmap_a);
+            tma_prefetch_desc(&tmap_w);
+            grid_dependency_wait();   // activations may come from the previous kernel
+            int issued = 0;
+            bool ok = true;
+            for (int kb = 0; kb < p.nkb && ok; ++kb) {
+                const int s = kb % kStages;
+                if (kb >= kStages)
+                    ok = mbar_wait(&empty[s], uint32_t(kb / kStages - 1) & 1u, &g_status, 10);
+                if (!ok) break;
+                mbar_arrive_expect_tx(&full[s], L::kActBytes + (DENSE ? kWtBytes : kPkBytes));
+                tma_load_2d(act_tile(s), &tmap_a, &full[s], kb * kBK, m0);
+                if constexpr (DENSE) tma_load_2d(wt_tile(s), &tmap_w, &full[s], kb * kBK, n0);
+                else tma_load_2d(pk_tile(s), &tmap_w, &full[s], kb * (kBK / 8), n0);
+                ++issued;
+            }
+            // copies still in flight must land before the CTA can retire
+            for (int kb = max(0, issued - kStages); kb < issued; ++kb)
+                mbar_wait(&full[kb % kStages], uint32_t(kb / kStages) & 1u, &g_status, 11);
+        }
+    } else if (warp == 5) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_f16(BF16, kBM, BT);
+            bool ok = true;
+            for (int kb = 0; kb < p.nkb && ok; ++kb) {
+                const int s = kb % kStages;
+                const uint32_t par = uint32_t(kb / kStages) & 1u;
+                ok = mbar_wait(&full[s], par, &g_status, 12);
+                if (ok && !DENSE) ok = mbar_wait(&dq_full[s], par, &g_status, 13);
+                if (!ok) break;
+                tc_fence_after();
+                const uint64_t a_desc = smem_desc_sw128(wt_tile(s));
+                const uint64_t b_desc = smem_desc_sw128(act_tile(s));
+#pragma unroll
+                for (int k = 0; k < kBK / 16; ++k)   // 16 K-values = 32 bytes = 2 descriptor units
+                    umma_f16_ss(tmem_d, a_desc + 2 * k, b_desc + 2 * k, idesc, (kb | k) != 0);
+                umma_commit(&empty[s]);
+            }
+            if (ok) umma_commit(acc_full);
+        }
+    } else {
+        // ---------------- dequantisers (warps 0-3), then epilogue ----------------
+        const int row = tid;                 // weight row within the tile
+        const int n = n0 + row;
+        const bool row_ok = n < p.N;
+        bool ok = true;
+        if constexpr (!DENSE) {
+            for (int kb = 0; kb < p.nkb; ++kb) {
+                const int s = kb % kStages;
+                // warp-uniform outcome: the warp leaves the loop together or not at all
+                ok = __all_sync(0xffffffffu, mbar_wait(&full[s], uint32_t(kb / kStages) & 1u, &g_status, 14));
+                if (!ok) break;
+                const uint4* src = reinterpret_cast<const uint4*>(pk_tile(s) + row * 32);
+                const uint4 wa = src[0], wb = src[1];
+                const uint32_t words[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+                // words 0-3 (K-values kb*64 + 0..31) and 4-7 (+32..63) each lie in one
+                // group because every group size is a multiple of 32
+                const int k0 = kb * kBK;
+                const int ga = min(k0 / p.g_eff, p.ng - 1);
+                const int gb = min((k0 + 32) / p.g_eff, p.ng - 1);
+                uint32_t s2a = 0, s2b = 0;
+                int za = 8, zb = 8;
+                if (row_ok) {
+                    const uint32_t sa = __ldg(p.scales + size_t(n) * p.ng + ga);
+                    const uint32_t sb = __ldg(p.scales + size_t(n) * p.ng + gb);
+                    s2a = sa | (sa << 16);
+                    s2b = sb | (sb << 16);
+                    if constexpr (ZP) {
+                        za = (__ldg(p.zeros + size_t(n >> 3) * p.ng + ga) >> (4 * (n & 7))) & 0xF;
+                        zb = (__ldg(p.zeros + size_t(n >> 3) * p.ng + gb) >> (4 * (n & 7))) & 0xF;
+                    }
+                }
+                const ZeroConst zca = make_zero_const<BF16>(za);
+                const ZeroConst zcb = make_zero_const<BF16>(zb);
+                uint8_t* dst = wt_tile(s) + row * 128;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    uint32_t q[4];
+                    unpack_word<BF16>(words[j], j < 4 ? zca : zcb, q);
+                    const uint32_t s2 = j < 4 ? s2a : s2b;
+                    uint4 o;
+                    o.x = scale_pair<BF16>(q[0], s2);
+                    o.y = scale_pair<BF16>(q[1], s2);
+                    o.z = scale_pair<BF16>(q[2], s2);
+                    o.w = scale_pair<BF16>(q[3], s2);
+                    // 16-byte chunk j of this 128-byte row goes to chunk j ^ (row % 8)
+                    *reinterpret_cast<uint4*>(dst + ((j ^ (row & 7)) << 4)) = o;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&dq_full[s]);
+            }
+        }
+        // ---------------- epilogue ----------------
+        if (ok) ok = mbar_wait(acc_full, 0u, &g_status, 15);
+        ok = __all_sync(0xffffffffu, ok);   // tcgen05.ld below is warp-collective
+        tc_fence_after();
+        if (ok) {
+            const uint32_t lane_base = uint32_t(32 * warp) << 16;
+#pragma unroll 1
+            for (int c = 0; c < BT / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(tmem_d + lane_base + uint32_t(32 * c), r);
+                tmem_ld_wait();
+                if (row_ok) {
+                    const int tok0 = m0 + 32 * c;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int tok = tok0 + j;
+                        if (tok < p.M) p.C[size_t(tok) * p.N + n] = from_f32<BF16>(__uint_as_float(r[j]));
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) tmem_dealloc(tmem_d, BT);
+}
+
+template <bool BF16, bool ZP, int BT, bool DENSE>
+cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tw, const Params& p,
+                     cudaStream_t stream) {
+    auto kern = prefill_kernel<BF16, ZP, BT, DENSE>;
+    constexpr int smem = Layout<BT, DENSE>::kBytes;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((p.N + kBM - 1) / kBM, (p.M + BT - 1) / BT);
+    kern<<<grid, kThreads, smem, stream>>>(ta, tw, p);
+    return cudaGetLastError();
+}
+
+template <int BT>
+cudaError_t launch_bt(const CUtensorMap& ta, const CUtensorMap& tw, const Params& p, bool bf16,
+                      bool zp, bool dense, cudaStream_t stream) {
+    if (dense) return bf16 ? launch_t<true, false, BT, true>(ta, tw, p, stream)
+                           : launch_t<false, false, BT, true>(ta, tw, p, stream);
+    if (bf16) return zp ? launch_t<true, true, BT, false>(ta, tw, p, stream)
+                        : launch_t<true, false, BT, false>(ta, tw, p, stream);
+    return zp ? launch_t<false, true, BT, false>(ta, tw, p, stream)
+              : launch_t<false, false, BT, false>(ta, tw, p, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const CUtensorMap& tmap_a, const CUtensorMap& tmap_w,
+                           const void* scales, const int32_t* zeros, void* C,
+                           const LayerShape& s, bool dense, int token_tile,
+                           cudaStream_t stream) {
+    Params p;
+    p.scales = static_cast<const uint16_t*>(scales);
+    p.zeros = zeros;
+    p.C = static_cast<uint16_t*>(C);
+    p.M = int(s.M);
+    p.N = int(s.N);
+    p.K = int(s.K);
+    p.g_eff = int(s.g_eff);
+    p.ng = int(s.ng);
+    p.nkb = int((s.K + kBK - 1) / kBK);
+    switch (token_tile) {
+        case 64: return launch_bt<64>(tmap_a, tmap_w, p, s.bf16, s.zp, dense, stream);
+        case 128: return launch_bt<128>(tmap_a, tmap_w, p, s.bf16, s.zp, dense, stream);
+        default: return launch_bt<256>(tmap_a, tmap_w, p, s.bf16, s.zp, dense, stream);
+    }
+}
+
+int take_status_prefill() {
+    int v = 0, z = 0;
+    if (cudaMemcpyFromSymbol(&v, g_status, sizeof(int)) != cudaSuccess) return -1;
+    if (v) cudaMemcpyToSymbol(g_status, &z, sizeof(int));
+    return v;
+}
+
+}  // namespace w4a16

@@ -1,0 +1,350 @@
+// C ABI of libw4a16 (declarations and argument contracts: include/w4a16.h).
+//
+// Host side only: argument validation (the rules of the pages' can_implement
+// and asserts), the M-router (_rdna_hybrid_w4a16_apply_impl's role), TMA
+// tensor-map encoding, and kernel launches on the caller's stream.  Nothing
+// here allocates device memory.
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/w4a16.h"
+#include "internal.h"
+
+namespace w4a16 {
+bool plan_decode(int64_t M, int64_t N, int64_t K, int num_sms, int* ks_out, int* stages_out,
+                 size_t* smem_out, int* nt_out);
+}
+
+namespace {
+
+using namespace w4a16;
+
+thread_local char g_err[512] = "";
+
+w4a16_status fail(w4a16_status code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+w4a16_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(W4A16_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Shape / enum checks shared by every entry point that takes a quantised weight.
+w4a16_status check_weight(int64_t N, int64_t K, int G, int qtype, int dtype, LayerShape* s) {
+    if (dtype != W4A16_FP16 && dtype != W4A16_BF16)
+        return fail(W4A16_ERR_INVALID_ARG, "dtype %d is not fp16 (0) or bf16 (1)", dtype);
+    if (qtype != W4A16_UINT4B8 && qtype != W4A16_UINT4)
+        return fail(W4A16_ERR_INVALID_ARG, "quant type %d is not uint4b8 (0) or uint4 (1)", qtype);
+    if (G != -1 && G != 32 && G != 64 && G != 128 && G != 256)
+        return fail(W4A16_ERR_INVALID_ARG, "group size %d not supported; supported: -1, 32, 64, 128, 256", G);
+    if (N < 1 || N > kMaxDim) return fail(W4A16_ERR_INVALID_ARG, "N=%lld out of range", (long long)N);
+    if (K < 16 || K > kMaxDim) return fail(W4A16_ERR_INVALID_ARG, "K=%lld out of range", (long long)K);
+    if (K % 16 != 0) return fail(W4A16_ERR_INVALID_ARG, "K=%lld must be divisible by 16", (long long)K);
+    const int64_t g_eff = G == -1 ? K : G;
+    if (K % g_eff != 0)
+        return fail(W4A16_ERR_INVALID_ARG, "K=%lld must be divisible by group_size=%d", (long long)K, G);
+    if (qtype == W4A16_UINT4 && N % 8 != 0)
+        return fail(W4A16_ERR_INVALID_ARG, "N must be divisible by 8 for packed zero points, got %lld", (long long)N);
+    if (s) {
+        s->N = N;
+        s->K = K;
+        s->g_eff = g_eff;
+        s->ng = K / g_eff;
+        s->ldq = (K / 8 + 3) / 4 * 4;
+        s->bf16 = dtype == W4A16_BF16;
+        s->zp = qtype == W4A16_UINT4;
+        s->M = 0;
+    }
+    return W4A16_OK;
+}
+
+w4a16_status check_qptrs(const void* Wq, const void* scales, const int32_t* zeros, int qtype) {
+    if (!Wq || !aligned(Wq, 16)) return fail(W4A16_ERR_INVALID_ARG, "Wq must be a non-null 16-byte aligned device pointer");
+    if (!scales || !aligned(scales, 2)) return fail(W4A16_ERR_INVALID_ARG, "scales must be a non-null 2-byte aligned device pointer");
+    if (qtype == W4A16_UINT4) {
+        if (!zeros || !aligned(zeros, 4)) return fail(W4A16_ERR_INVALID_ARG, "uint4 needs a non-null 4-byte aligned zeros pointer");
+    } else if (zeros) {
+        return fail(W4A16_ERR_INVALID_ARG, "zeros must be NULL for uint4b8 (the zero point is the constant 8)");
+    }
+    return W4A16_OK;
+}
+
+// --- TMA tensor maps -------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+cudaError_t g_encode_err = cudaSuccess;
+
+w4a16_status get_encoder() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        g_encode_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                        cudaEnableDefault, &q);
+        if (g_encode_err == cudaSuccess && q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        else if (g_encode_err == cudaSuccess)
+            g_encode_err = cudaErrorSymbolNotFound;
+    });
+    if (!g_encode) return cuda_fail(g_encode_err, "cuTensorMapEncodeTiled lookup");
+    return W4A16_OK;
+}
+
+// 2-D row-major tensor [rows][cols] of `elem` bytes, box [box_rows][box_cols].
+w4a16_status make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem,
+                      uint64_t cols, uint64_t rows, uint64_t row_stride_bytes, uint32_t box_cols,
+                      uint32_t box_rows, CUtensorMapSwizzle swz) {
+    w4a16_status st = get_encoder();
+    if (st) return st;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {row_stride_bytes};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    (void)elem;
+    CUresult r = g_encode(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(W4A16_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d) for a %llux%llu tensor",
+                    int(r), (unsigned long long)rows, (unsigned long long)cols);
+    return W4A16_OK;
+}
+
+// --- device properties ------------------------------------------------------
+w4a16_status device_sms(int* sms) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    static std::mutex mu;
+    static int cache[64] = {0};
+    std::lock_guard<std::mutex> lk(mu);
+    if (dev >= 0 && dev < 64 && cache[dev]) {
+        *sms = cache[dev];
+        return W4A16_OK;
+    }
+    int v = 0;
+    e = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    if (dev >= 0 && dev < 64) cache[dev] = v;
+    *sms = v;
+    return W4A16_OK;
+}
+
+// --- router -----------------------------------------------------------------
+// Crossover points measured on GB300 (decode kernel vs fused tcgen05 kernel);
+// the dense copy wins over fused dequant only where the tensor pipe, not the
+// dequantisation, limits the fused kernel.
+constexpr int64_t kDecodeUpToM = 32;
+constexpr int64_t kDenseFromM = 1024;
+
+int route_impl(int64_t M, int64_t N, int64_t K, bool has_dense) {
+    if (M <= kDecodeUpToM) {
+        int ks, stages, nt;
+        size_t smem;
+        if (plan_decode(M, N, K, 152, &ks, &stages, &smem, &nt)) return W4A16_PATH_DECODE;
+    }
+    if (has_dense && M >= kDenseFromM) return W4A16_PATH_DENSE;
+    return W4A16_PATH_FUSED;
+}
+
+int token_tile_for(int64_t M) {
+    if (M <= 64) return 64;
+    if (M <= 128) return 128;
+    return 256;
+}
+
+w4a16_status launch_tcgen05(const void* A, const void* Wsrc, bool dense, const void* scales,
+                            const int32_t* zeros, void* C, const LayerShape& s,
+                            cudaStream_t stream) {
+    const int bt = token_tile_for(s.M);
+    CUtensorMap ta, tw;
+    w4a16_status st = make_map(&ta, A, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, uint64_t(s.K),
+                               uint64_t(s.M), uint64_t(s.K) * 2, 64, uint32_t(bt),
+                               CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st) return st;
+    if (dense)
+        st = make_map(&tw, Wsrc, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, uint64_t(s.K), uint64_t(s.N),
+                      uint64_t(s.K) * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+    else
+        st = make_map(&tw, Wsrc, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, uint64_t(s.ldq), uint64_t(s.N),
+                      uint64_t(s.ldq) * 4, 8, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (st) return st;
+    cudaError_t e = launch_prefill(ta, tw, scales, zeros, C, s, dense, bt, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "tcgen05 GEMM launch");
+    return W4A16_OK;
+}
+
+w4a16_status launch_decode_path(const void* A, const void* Wq, const void* scales,
+                                const int32_t* zeros, void* C, const LayerShape& s,
+                                cudaStream_t stream) {
+    int sms = 0;
+    w4a16_status st = device_sms(&sms);
+    if (st) return st;
+    CUtensorMap tq;
+    st = make_map(&tq, Wq, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, uint64_t(s.ldq), uint64_t(s.N),
+                  uint64_t(s.ldq) * 4, 32, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st) return st;
+    cudaError_t e = launch_decode(tq, A, scales, zeros, C, s, sms, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "decode GEMM launch");
+    return W4A16_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int w4a16_version(void) { return 100; }
+
+const char* w4a16_last_error_string(void) { return g_err; }
+
+w4a16_status w4a16_packed_layout(int64_t N, int64_t K, int G, int qtype, int dtype,
+                                 size_t* total_bytes, size_t* scales_off, size_t* zeros_off,
+                                 int64_t* ldq_words) {
+    LayerShape s;
+    w4a16_status st = check_weight(N, K, G, qtype, dtype, &s);
+    if (st) return st;
+    const size_t q_bytes = size_t(N) * size_t(s.ldq) * 4;
+    const size_t so = round_up(q_bytes, 256);
+    const size_t s_bytes = size_t(N) * size_t(s.ng) * 2;
+    size_t zo = 0, end = so + s_bytes;
+    if (s.zp) {
+        zo = round_up(end, 256);
+        end = zo + size_t(N / 8) * size_t(s.ng) * 4;
+    }
+    if (total_bytes) *total_bytes = round_up(end, 256);
+    if (scales_off) *scales_off = so;
+    if (zeros_off) *zeros_off = zo;
+    if (ldq_words) *ldq_words = s.ldq;
+    g_err[0] = '\0';
+    return W4A16_OK;
+}
+
+w4a16_status w4a16_pack(const uint8_t* q, const void* scales, const int32_t* zeros, void* Wpacked,
+                        int64_t N, int64_t K, int G, int qtype, int dtype, void* stream) {
+    LayerShape s;
+    w4a16_status st = check_weight(N, K, G, qtype, dtype, &s);
+    if (st) return st;
+    if (!q || !aligned(q, 8)) return fail(W4A16_ERR_INVALID_ARG, "q must be a non-null 8-byte aligned device pointer");
+    if (!Wpacked || !aligned(Wpacked, 256)) return fail(W4A16_ERR_INVALID_ARG, "Wpacked must be a non-null 256-byte aligned device pointer");
+    if (!scales || !aligned(scales, 2)) return fail(W4A16_ERR_INVALID_ARG, "scales must be a non-null 2-byte aligned device pointer");
+    if (s.zp && (!zeros || !aligned(zeros, 4))) return fail(W4A16_ERR_INVALID_ARG, "uint4 needs a non-null 4-byte aligned zeros pointer");
+    if (!s.zp && zeros) return fail(W4A16_ERR_INVALID_ARG, "zeros must be NULL for uint4b8 (the zero point is the constant 8)");
+    size_t total, so, zo;
+    w4a16_packed_layout(N, K, G, qtype, dtype, &total, &so, &zo, nullptr);
+    uint8_t* base = static_cast<uint8_t*>(Wpacked);
+    cudaError_t e = launch_pack(q, scales, zeros, base, base + so, s.zp ? base + zo : nullptr, s,
+                                static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "pack launch");
+    g_err[0] = '\0';
+    return W4A16_OK;
+}
+
+int w4a16_route(int64_t M, int64_t N, int64_t K, int G, int qtype, int dtype, int has_dense) {
+    if (check_weight(N, K, G, qtype, dtype, nullptr) != W4A16_OK) return -1;
+    if (M < 0 || M > kMaxDim) return -1;
+    return route_impl(M, N, K, has_dense != 0);
+}
+
+w4a16_status w4a16_gemm_ex(const void* A, const void* Wq, const void* scales,
+                           const int32_t* zeros, const void* Wdense, void* C, int64_t M,
+                           int64_t N, int64_t K, int G, int qtype, int dtype, int path,
+                           void* stream) {
+    LayerShape s;
+    w4a16_status st = check_weight(N, K, G, qtype, dtype, &s);
+    if (st) return st;
+    if (M < 0 || M > kMaxDim) return fail(W4A16_ERR_INVALID_ARG, "M=%lld out of range", (long long)M);
+    if (path < W4A16_PATH_AUTO || path > W4A16_PATH_DENSE) return fail(W4A16_ERR_INVALID_ARG, "unknown path %d", path);
+    st = check_qptrs(Wq, scales, zeros, qtype);
+    if (st) return st;
+    if (!A || !aligned(A, 16)) return fail(W4A16_ERR_INVALID_ARG, "A must be a non-null 16-byte aligned device pointer");
+    if (!C || !aligned(C, 2)) return fail(W4A16_ERR_INVALID_ARG, "C must be a non-null 2-byte aligned device pointer");
+    if (Wdense && !aligned(Wdense, 16)) return fail(W4A16_ERR_INVALID_ARG, "Wdense must be 16-byte aligned");
+    s.M = M;
+    if (path == W4A16_PATH_AUTO) path = route_impl(M, N, K, Wdense != nullptr);
+    if (path == W4A16_PATH_DENSE && !Wdense) return fail(W4A16_ERR_INVALID_ARG, "the dense path needs a dense copy (Wdense)");
+    if (path == W4A16_PATH_DECODE) {
+        int ks, stages, nt;
+        size_t smem;
+        if (M > kDecodeMaxM) return fail(W4A16_ERR_INVALID_ARG, "the decode path takes M <= %lld", (long long)kDecodeMaxM);
+        if (M > 0 && !plan_decode(M, N, K, 152, &ks, &stages, &smem, &nt))
+            return fail(W4A16_ERR_UNSUPPORTED, "decode path: the activation slice for M=%lld, K=%lld does not fit in shared memory", (long long)M, (long long)K);
+    }
+    g_err[0] = '\0';
+    if (M == 0) return W4A16_OK;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (path == W4A16_PATH_DECODE) return launch_decode_path(A, Wq, scales, zeros, C, s, cs);
+    if (path == W4A16_PATH_DENSE) return launch_tcgen05(A, Wdense, true, nullptr, nullptr, C, s, cs);
+    return launch_tcgen05(A, Wq, false, scales, zeros, C, s, cs);
+}
+
+w4a16_status w4a16_gemm(const void* A, const void* Wq, const void* scales, const int32_t* zeros,
+                        void* C, int64_t M, int64_t N, int64_t K, int G, int qtype, int dtype,
+                        void* stream) {
+    return w4a16_gemm_ex(A, Wq, scales, zeros, nullptr, C, M, N, K, G, qtype, dtype,
+                         W4A16_PATH_AUTO, stream);
+}
+
+w4a16_status w4a16_dequant(const void* Wq, const void* scales, const int32_t* zeros, void* W,
+                           int64_t N, int64_t K, int G, int qtype, int dtype, void* stream) {
+    LayerShape s;
+    w4a16_status st = check_weight(N, K, G, qtype, dtype, &s);
+    if (st) return st;
+    st = check_qptrs(Wq, scales, zeros, qtype);
+    if (st) return st;
+    if (!W || !aligned(W, 16)) return fail(W4A16_ERR_INVALID_ARG, "W must be a non-null 16-byte aligned device pointer");
+    cudaError_t e = launch_dequant(static_cast<const uint32_t*>(Wq), scales, zeros, W, s,
+                                   static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "dequant launch");
+    g_err[0] = '\0';
+    return W4A16_OK;
+}
+
+w4a16_status w4a16_gemm_dense(const void* A, const void* W, void* C, int64_t M, int64_t N,
+                              int64_t K, int dtype, void* stream) {
+    if (dtype != W4A16_FP16 && dtype != W4A16_BF16)
+        return fail(W4A16_ERR_INVALID_ARG, "dtype %d is not fp16 (0) or bf16 (1)", dtype);
+    if (M < 0 || M > kMaxDim) return fail(W4A16_ERR_INVALID_ARG, "M=%lld out of range", (long long)M);
+    if (N < 1 || N > kMaxDim) return fail(W4A16_ERR_INVALID_ARG, "N=%lld out of range", (long long)N);
+    if (K < 16 || K > kMaxDim || K % 16) return fail(W4A16_ERR_INVALID_ARG, "K=%lld must be a positive multiple of 16", (long long)K);
+    if (!A || !aligned(A, 16)) return fail(W4A16_ERR_INVALID_ARG, "A must be a non-null 16-byte aligned device pointer");
+    if (!W || !aligned(W, 16)) return fail(W4A16_ERR_INVALID_ARG, "W must be a non-null 16-byte aligned device pointer");
+    if (!C || !aligned(C, 2)) return fail(W4A16_ERR_INVALID_ARG, "C must be a non-null 2-byte aligned device pointer");
+    g_err[0] = '\0';
+    if (M == 0) return W4A16_OK;
+    LayerShape s;
+    s.M = M;
+    s.N = N;
+    s.K = K;
+    s.g_eff = K;
+    s.ng = 1;
+    s.ldq = (K / 8 + 3) / 4 * 4;
+    s.bf16 = dtype == W4A16_BF16;
+    s.zp = false;
+    return launch_tcgen05(A, W, true, nullptr, nullptr, C, s, static_cast<cudaStream_t>(stream));
+}
+
+w4a16_status w4a16_device_status(int* site) {
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    int v = take_status_decode();
+    if (v == 0) v = take_status_prefill();
+    if (site) *site = v > 0 ? v : 0;
+    if (v < 0) return fail(W4A16_ERR_CUDA, "reading the device status word failed");
+    if (v > 0) return fail(W4A16_ERR_DEVICE_TIMEOUT, "a kernel barrier wait timed out at site %d", v);
+    return W4A16_OK;
+}
+
+}  // extern "C"
