@@ -1,0 +1,568 @@
+#!/usr/bin/env python
+"""Benchmark of the W4A16 int4-weight linear layer on GB300.
+
+Default workload: decode GEMV on a 7B attention-projection shape,
+M in {1, 4, 8}, K = N = 4096, group size 128, uint4b8, bf16 activations,
+seeded synthetic weights and activations.  One step runs the layer for each of
+the three M values on each of L = 32 distinct weight copies (32 x 8.65 MB =
+277 MB > the 129 MB L2), so every step streams its weights from HBM, like a
+decode pass over a stack of layers.
+
+Prints one JSON line (rank 0).  `value` is whole-job weight throughput
+(packed q + scale bytes per second) with inputs resident in HBM, from CUDA
+events around K replays of a CUDA graph of one step; `e2e` is the same metric
+through the C ABI called eagerly with the activations copied from pinned host
+memory and the outputs copied back inside the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+`--impl reference` times the CPU oracle (the plain float64 definition, from
+oracle/) on a bounded sample of the same workload.  With several GPUs
+(torchrun) every rank runs its own replica of the workload (no data exchange;
+weak scaling) and rank 0 reports the aggregate.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "W4A16 GEMM TFLOP/s and weight GB/s vs M; % of HBM / bf16 tensor roofline"
+WORKLOAD = "decode_gemv_k4096_n4096_g128_uint4b8_bf16_m1_4_8"
+MS = (1, 4, 8)
+N_, K_, G_ = 4096, 4096, 128
+QTYPE, DTYPE = "uint4b8", "bf16"
+LAYERS = 32
+L2_BYTES = 129 * 1024 * 1024
+
+
+def weight_bytes(N, K, G, zp):
+    ng = K // (K if G == -1 else G)
+    return N * K // 2 + N * ng * 2 + ((N // 8) * ng * 4 if zp else 0)
+
+
+def alg_bytes(M, N, K, G, zp):
+    return weight_bytes(N, K, G, zp) + M * K * 2 + M * N * 2
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extras", action="store_true", help="skip the prefill/zero-point side measurements")
+    ap.add_argument("--profile-case", choices=["decode", "zp", "prefill", "dense", "dequant"],
+                    help="only run `--reps` eager launches of one kernel (for ncu), then exit")
+    ap.add_argument("--reps", type=int, default=8)
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; replicas only)
+# ---------------------------------------------------------------------------
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.out = ""
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for ln in self.out.strip().splitlines():
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[4:8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        seen = set()
+        for _, _, flags in rows:
+            for nm, f in zip(names, flags):
+                if f.lower() == "active":
+                    seen.add(nm)
+        # samples taken while the GPU was busy (clock above idle) describe the load
+        busy = [r for r in rows if r[0] > 0.5 * r[1]] or rows
+        return {"sm_mhz": statistics.median(r[0] for r in busy), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": sorted(seen), "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# ncu-derived DRAM traffic of the dominant kernel, if taken on the current source
+# ---------------------------------------------------------------------------
+def kernel_source_hash(names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "w4a16_int4_weight_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(summary_name, sources, scale):
+    """Bytes per launch from a profiles/ summary, or None if the kernel changed."""
+    path = os.path.join(ROOT, "profiles", summary_name)
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    mh = re.search(r"source hash:\s*([0-9a-f]{16})", text)
+    mt = re.search(r"dram bytes per launch \(read \+ write\):\s*([0-9]+)", text)
+    if not mh or not mt or mh.group(1) != kernel_source_hash(sources):
+        return None
+    return int(mt.group(1)) * scale
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained"), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline / reference arm)
+# ---------------------------------------------------------------------------
+_ORACLE_INPUTS = {}
+
+
+def oracle_inputs(layer):
+    """Seeded inputs of one layer (generated once, outside any timed region)."""
+    if layer not in _ORACLE_INPUTS:
+        import oracle as orc
+        from w4a16_int4_weight_gb300 import inputs as synth
+        p = synth.Problem(max(MS), N_, K_, G_, QTYPE, DTYPE, seed=layer)
+        q, s, _ = synth.make_weights(p)
+        _ORACLE_INPUTS[layer] = (orc.pack_q(q), s, synth.make_activations(p))
+    return _ORACLE_INPUTS[layer]
+
+
+def oracle_sample(n_cols, layer=0):
+    """Time the oracle on the first n_cols output columns of one layer, for each
+    of the three M.  Returns (seconds, weight bytes processed)."""
+    import oracle as orc
+    words, s, A = oracle_inputs(layer)
+    rows = np.arange(max(MS))
+    total_t, total_b = 0.0, 0
+    for M in MS:
+        t0 = time.perf_counter()
+        orc.linear_rows_packed(A, words[:n_cols], K_, s[:n_cols], None, rows[:M], G_, DTYPE)
+        total_t += time.perf_counter() - t0
+        total_b += weight_bytes(n_cols, K_, G_, False)
+    return total_t, total_b
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    import oracle as orc
+    orc.build()
+    # size each step so that warmup + steps stay within about two minutes
+    t, b = oracle_sample(256)
+    per_step_budget = 100.0 / max(1, args.steps + args.warmup)
+    n_cols = int(max(8, min(N_, 256 * per_step_budget / max(t, 1e-6))) // 8 * 8)
+    for _ in range(args.warmup):
+        oracle_sample(n_cols)
+    tt, bb = 0.0, 0
+    for _ in range(args.steps):
+        t, b = oracle_sample(n_cols)
+        tt += t
+        bb += b
+    value = bb / tt / 1e9
+    sample = (f"oracle (unpack -> dequant -> float64 GEMM) on output columns 0..{n_cols - 1} of one "
+              f"layer for M = 1, 4, 8 per step")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded SplitMix64)",
+        "config": {"workload": WORKLOAD, "M": list(MS), "K": K_, "N": N_, "group_size": G_,
+                   "qtype": QTYPE, "act_dtype": DTYPE},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": orc.num_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def make_layers(torch, B, synth, n_layers, M_max, N, K, G, qtype, dtype, seed0=0):
+    tdt = {"fp16": torch.float16, "bf16": torch.bfloat16}[dtype]
+    layers = []
+    tot, so, zo, _ = B.packed_layout(N, K, G, qtype, dtype)
+    for l in range(n_layers):
+        p = synth.Problem(M_max, N, K, G, qtype, dtype, seed=seed0 + l)
+        q, s, z = synth.make_weights(p)
+        qd = torch.from_numpy(q).cuda()
+        sd = torch.from_numpy(s.view(np.int16)).cuda().view(tdt)
+        zd = torch.from_numpy(z).cuda() if z is not None else None
+        buf = torch.empty(tot, dtype=torch.uint8, device="cuda")
+        B.pack(qd, sd, zd, buf, N, K, G, qtype, dtype)
+        base = buf.data_ptr()
+        layers.append((buf, base, base + so, base + zo if z is not None else None))
+    torch.cuda.synchronize()
+    return layers
+
+
+def time_graph(torch, fn, reps, warmup):
+    stream = torch.cuda.current_stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / 1e3 / reps
+
+
+def extras(torch, B, synth, peaks):
+    """Side measurements on the other workloads (not the headline): the prefill
+    tcgen05 kernel (fused and dense) and the zero-point decode pair."""
+    hbm, tc_burst, _, kind = peaks
+    out = {}
+    tdt = torch.bfloat16
+    # prefill M=2048, K=4096, N=14336, G=128, uint4b8: 4 weight copies rotate
+    M, N, K, G = 2048, 14336, 4096, 128
+    lay = make_layers(torch, B, synth, 4, M, N, K, G, "uint4b8", "bf16", seed0=100)
+    A = torch.randn(M, K, device="cuda").to(tdt)
+    Cs = [torch.empty(M, N, dtype=tdt, device="cuda") for _ in lay]
+    dense = []
+    for (_, wq, sp, _) in lay:
+        W = torch.empty(N, K, dtype=tdt, device="cuda")
+        B.dequant(wq, sp, None, W, N, K, G, "uint4b8", "bf16")
+        dense.append(W)
+    flops = 2.0 * M * N * K
+
+    def run(path):
+        for i, (_, wq, sp, _) in enumerate(lay):
+            B.gemm_ex(A, wq, sp, None, dense[i] if path == "dense" else None, Cs[i], M, N, K, G,
+                      "uint4b8", "bf16", path)
+    for path in ("fused", "dense"):
+        t = time_graph(torch, lambda: run(path), 10, 3) / len(lay)
+        out[f"prefill_{path}_m2048_k4096_n14336"] = {
+            "tflops": flops / t / 1e12, "us": t * 1e6,
+            "frac_of_bf16_peak": flops / t / 1e12 / tc_burst, "peak_kind": kind}
+    # dequant kernel on the same layer: HBM-bound (write 2 B, read 0.5 B per weight)
+    (_, wq, sp, _) = lay[0]
+
+    def deq():
+        for i, (_, wq_, sp_, _) in enumerate(lay):
+            B.dequant(wq_, sp_, None, dense[i], N, K, G, "uint4b8", "bf16")
+    t = time_graph(torch, deq, 10, 3) / len(lay)
+    byts = weight_bytes(N, K, G, False) + N * K * 2
+    out["dequant_k4096_n14336"] = {"gbs": byts / t / 1e9, "frac_of_hbm": byts / t / 1e9 / hbm}
+    del lay, dense, Cs
+    torch.cuda.empty_cache()
+    # zero-point decode pair: M=16, G=32, uint4, K/N = 4096/11008 and 11008/4096
+    for (K, N) in ((4096, 11008), (11008, 4096)):
+        M, G = 16, 32
+        lay = make_layers(torch, B, synth, 8, M, N, K, G, "uint4", "bf16", seed0=200)
+        A = torch.randn(M, K, device="cuda").to(tdt)
+        C = torch.empty(M, N, dtype=tdt, device="cuda")
+
+        def run_zp():
+            for (_, wq, sp, zp) in lay:
+                B.gemm_ex(A, wq, sp, zp, None, C, M, N, K, G, "uint4", "bf16", "auto",
+                          static_weights=True)
+        t = time_graph(torch, run_zp, 200, 10) / len(lay)
+        byts = alg_bytes(M, N, K, G, True)
+        out[f"decode_zp_m16_g32_k{K}_n{N}"] = {"gbs": byts / t / 1e9, "frac_of_hbm": byts / t / 1e9 / hbm,
+                                               "us": t * 1e6}
+        del lay
+        torch.cuda.empty_cache()
+    return out
+
+
+def profile_case(args):
+    """Eager launches of one kernel on its workload, nothing timed (an ncu target)."""
+    import torch
+    torch.cuda.set_device(0)
+    from w4a16_int4_weight_gb300 import build as wbuild
+    wbuild.build()
+    from w4a16_int4_weight_gb300 import binding as B
+    from w4a16_int4_weight_gb300 import inputs as synth
+    tdt = torch.bfloat16
+    c = args.profile_case
+    if c in ("decode", "zp"):
+        M, N, K, G, qt = (8, N_, K_, G_, QTYPE) if c == "decode" else (16, 11008, 4096, 32, "uint4")
+        lay = make_layers(torch, B, synth, 4, M, N, K, G, qt, "bf16")
+        A = torch.randn(M, K, device="cuda").to(tdt)
+        C = torch.empty(M, N, dtype=tdt, device="cuda")
+        for r in range(args.reps):
+            _, wq, sp, zp = lay[r % len(lay)]
+            B.gemm(A, wq, sp, zp, C, M, N, K, G, qt, "bf16")
+    else:
+        M, N, K, G = 2048, 14336, 4096, 128
+        lay = make_layers(torch, B, synth, 1, M, N, K, G, "uint4b8", "bf16", seed0=100)
+        _, wq, sp, _ = lay[0]
+        A = torch.randn(M, K, device="cuda").to(tdt)
+        C = torch.empty(M, N, dtype=tdt, device="cuda")
+        W = torch.empty(N, K, dtype=tdt, device="cuda")
+        B.dequant(wq, sp, None, W, N, K, G, "uint4b8", "bf16")
+        for _ in range(args.reps):
+            if c == "dequant":
+                B.dequant(wq, sp, None, W, N, K, G, "uint4b8", "bf16")
+            else:
+                B.gemm_ex(A, wq, sp, None, W if c == "dense" else None, C, M, N, K, G, "uint4b8",
+                          "bf16", "dense" if c == "dense" else "fused")
+    torch.cuda.synchronize()
+    code, site = B.device_status()
+    print(f"profile case {c}: {args.reps} launches, device status {code}")
+    return 0 if code == 0 else 1
+
+
+def main():
+    args = parse()
+    if args.profile_case:
+        return profile_case(args)
+    if args.impl == "reference":
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        return run_reference(args, world, rank)
+
+    import torch
+    world, rank, local = dist_setup()
+    from w4a16_int4_weight_gb300 import build as wbuild
+    if rank == 0 or not os.path.exists(wbuild.LIB):
+        wbuild.build()
+    barrier(world)
+    from w4a16_int4_weight_gb300 import binding as B
+    from w4a16_int4_weight_gb300 import inputs as synth
+
+    peaks = measured_peaks()
+    hbm_peak, tc_peak, _, peak_kind = peaks
+    tdt = torch.bfloat16
+    layers = make_layers(torch, B, synth, LAYERS, max(MS), N_, K_, G_, QTYPE, DTYPE)
+    A_host = {M: torch.from_numpy(synth.make_activations(synth.Problem(M, N_, K_, G_, QTYPE, DTYPE, seed=7)).view(np.int16)).view(tdt) for M in MS}
+    A_dev = {M: A_host[M].cuda() for M in MS}
+    C_dev = {M: torch.empty(LAYERS, M, N_, dtype=tdt, device="cuda") for M in MS}
+
+    # the packed weights are written once before timing and then only read, so
+    # the layer is called with the static-weights promise (W4A16_OPT_STATIC_WEIGHTS)
+    def gemm(M, l, wq, sp):
+        B.gemm_ex(A_dev[M], wq, sp, None, None, C_dev[M][l], M, N_, K_, G_, QTYPE, DTYPE, "auto",
+                  static_weights=True)
+
+    def step():
+        for M in MS:
+            for l, (_, wq, sp, _) in enumerate(layers):
+                gemm(M, l, wq, sp)
+
+    launches_per_step = len(MS) * LAYERS
+    wbytes_step = launches_per_step * weight_bytes(N_, K_, G_, False)
+    abytes_step = LAYERS * sum(alg_bytes(M, N_, K_, G_, False) for M in MS)
+    flops_step = LAYERS * sum(2.0 * M * N_ * K_ for M in MS)
+
+    # ---- device-resident timing: CUDA graph of one step, K replays ----
+    stream = torch.cuda.current_stream()
+    g = torch.cuda.CUDAGraph()
+    step()   # eager warm-up of every kernel instantiation before capture
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        step()
+    for _ in range(max(3, args.warmup)):
+        g.replay()
+    torch.cuda.synchronize()
+    gpu_uuid = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+    gpu_id = gpu_uuid if gpu_uuid.startswith("GPU-") else f"GPU-{gpu_uuid}"
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(gpu_id) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    t_dev = e0.elapsed_time(e1) / 1e3
+    t_max = max_over_ranks(t_dev, world)
+    ms_per_step = 1e3 * t_max / args.steps
+    value = world * args.steps * wbytes_step / t_max / 1e9
+
+    # per-M breakdown (graph of the 32 layers at one M)
+    per_m = {}
+    for M in MS:
+        def one_m(M=M):
+            for l, (_, wq, sp, _) in enumerate(layers):
+                gemm(M, l, wq, sp)
+        t = time_graph(torch, one_m, 300, 10) / LAYERS
+        per_m[str(M)] = {"us_per_launch": t * 1e6,
+                         "weight_gbs": weight_bytes(N_, K_, G_, False) / t / 1e9,
+                         "alg_gbs": alg_bytes(M, N_, K_, G_, False) / t / 1e9,
+                         "tflops": 2.0 * M * N_ * K_ / t / 1e12,
+                         "frac_of_hbm": alg_bytes(M, N_, K_, G_, False) / t / 1e9 / hbm_peak}
+
+    # ---- end to end through the C ABI: host activations in, host outputs out ----
+    A_pin = {M: A_host[M].pin_memory() for M in MS}
+    C_pin = {M: torch.empty(LAYERS, M, N_, dtype=tdt).pin_memory() for M in MS}
+    h2d = sum(A_pin[M].numel() * 2 for M in MS)
+    d2h = sum(C_pin[M].numel() * 2 for M in MS)
+    e2e_steps = max(1, min(args.steps, 300))
+
+    def e2e_step():
+        for M in MS:
+            A_dev[M].copy_(A_pin[M], non_blocking=True)
+            for l, (_, wq, sp, _) in enumerate(layers):
+                gemm(M, l, wq, sp)
+            C_pin[M].copy_(C_dev[M], non_blocking=True)
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_e2e = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+    e2e_value = world * e2e_steps * wbytes_step / t_e2e / 1e9
+
+    extra = {}
+    if rank == 0 and not args.no_extras:
+        extra = extras(torch, B, synth, peaks)
+
+    # roofline of the dominant kernel (the decode kernel: every launch in the step)
+    t_launch = t_dev / (args.steps * launches_per_step)
+    achieved = (abytes_step / launches_per_step) / t_launch / 1e9
+    traffic = profiled_traffic("decode_kernel_m1_4_8_k4096_n4096.md",
+                               ["decode.cu", "common.cuh"], 1)
+
+    cpu = None
+    if rank == 0:
+        import oracle as orc
+        orc.build()
+        # bounded sample: the oracle on whole layers until about 15 s of CPU time
+        tt, bb, nl = 0.0, 0, 0
+        while tt < 15.0 and nl < 4:
+            t, b = oracle_sample(N_, layer=nl)
+            tt += t
+            bb += b
+            nl += 1
+        cpu = {"value": bb / tt / 1e9, "unit": "GB/s", "cores": orc.num_threads(), "kind": "oracle",
+               "sample": f"{nl} whole layer(s) of the workload, M = 1, 4, 8 each "
+                         f"(unpack -> dequant -> float64 GEMM), {tt:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded SplitMix64 weights and activations)",
+            "config": {"workload": WORKLOAD, "M": list(MS), "K": K_, "N": N_, "group_size": G_,
+                       "qtype": QTYPE, "act_dtype": DTYPE, "layers_per_step": LAYERS,
+                       "l2": f"inputs larger than L2: {LAYERS} distinct weight copies, "
+                             f"{LAYERS * weight_bytes(N_, K_, G_, False) / 1e6:.0f} MB per pass",
+                       "timing": "CUDA graph of one step replayed K times, CUDA events",
+                       "call": "w4a16_gemm_ex(path=auto | W4A16_OPT_STATIC_WEIGHTS)",
+                       "parallelism": f"replicas x{world}"},
+            "tflops": world * args.steps * flops_step / t_max / 1e12,
+            "alg_gbs": world * args.steps * abytes_step / t_max / 1e9,
+            "per_m": per_m,
+            "gpu_launches": args.steps * launches_per_step,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved / hbm_peak, "traffic": traffic,
+                         "peak_kind": peak_kind, "kernel": "decode_kernel"},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+            "clocks": clk.summary(),
+            "extras": extra,
+        }
+        print(json.dumps(line), flush=True)
+    barrier(world)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

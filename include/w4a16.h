@@ -76,12 +76,20 @@ typedef enum {
  *                      the nibbles are v0,v2,v4,v6,v1,v3,v5,v7 (the pages'
  *                      ExLlama shuffle, unshuffle shifts 0,16,4,20,8,24,12,28).
  *                      Words j >= K/8 are zero.
- *   scales_off         scales: dtype [N][K/G_eff], row-major (a copy of the input).
- *   zeros_off          zero points (uint4 only): int32 [N/8][K/G_eff] (a copy).
+ *   scales_off         scales, transposed: dtype [K/G_eff][lds], lds = round_up(N, 8);
+ *                      element (g, n) is the scale of row n, group g.  Padding
+ *                      elements (n >= N) are zero.
+ *   zeros_off          zero points (uint4 only), transposed: int32 [K/G_eff][ldz],
+ *                      ldz = round_up(N/8, 4); word (g, j) holds the zero points
+ *                      of rows 8j .. 8j+7 of group g, row n at bits 4*(n%8).
+ *                      Padding words are zero.
  *
- * Each section starts on a 256-byte boundary; total_bytes is a multiple of 256.
- * zeros_off is 0 for uint4b8.  Host-only; returns W4A16_ERR_INVALID_ARG on bad
- * arguments.  Any output pointer may be NULL.
+ * The transposition puts the scales of 128 consecutive rows of one group in
+ * 256 contiguous bytes, so the kernels fetch them with the same TMA bulk
+ * copies that bring the weight tiles.  Each section starts on a 256-byte
+ * boundary; total_bytes is a multiple of 256.  zeros_off is 0 for uint4b8.
+ * Host-only; returns W4A16_ERR_INVALID_ARG on bad arguments.  Any output
+ * pointer may be NULL.
  */
 w4a16_status w4a16_packed_layout(int64_t N, int64_t K, int G, int qtype, int dtype,
                                  size_t* total_bytes, size_t* scales_off, size_t* zeros_off,
@@ -94,10 +102,10 @@ w4a16_status w4a16_packed_layout(int64_t N, int64_t K, int G, int qtype, int dty
  *  the triton_w4a16 page.)
  *   q        device uint8 [N][K], one value per byte in natural K order; only the
  *            low 4 bits of each byte are used.  8-byte aligned.
- *   scales   device dtype [N][K/G_eff].  2-byte aligned.
+ *   scales   device dtype [N][K/G_eff] (the checkpoint layout).  2-byte aligned.
  *   zeros    device int32 [N/8][K/G_eff] for uint4 (N % 8 == 0), NULL for uint4b8.
  *   Wpacked  device buffer of total_bytes (w4a16_packed_layout), 256-byte aligned,
- *            must not overlap the inputs.  Fully overwritten.
+ *            must not overlap the inputs.  Fully overwritten, padding included.
  * Enqueues one or two kernels on `stream`.
  */
 w4a16_status w4a16_pack(const uint8_t* q, const void* scales, const int32_t* zeros,
@@ -110,9 +118,10 @@ w4a16_status w4a16_pack(const uint8_t* q, const void* scales, const int32_t* zer
  * dequant GEMM for prefill).
  *   A        device dtype [M][K], row-major, contiguous (row stride K).  16-byte aligned.
  *   Wq       device q section of a packed buffer (its offset 0).  16-byte aligned.
- *   scales   device dtype [N][K/G_eff] (the packed buffer's scale section, or the
- *            caller's own array in that layout).  2-byte aligned.
- *   zeros    device int32 [N/8][K/G_eff] for uint4, NULL for uint4b8.  4-byte aligned.
+ *   scales   device scale section of the packed buffer (transposed [K/G_eff][lds],
+ *            see above), or the caller's own array in that layout.  16-byte aligned.
+ *   zeros    device zero-point section ([K/G_eff][ldz] int32) for uint4, NULL for
+ *            uint4b8.  16-byte aligned.
  *   C        device dtype [M][N], row-major, written in full, must not overlap inputs.
  *            2-byte aligned.
  *   M        >= 0; M == 0 returns W4A16_OK and enqueues nothing.
@@ -123,12 +132,27 @@ w4a16_status w4a16_gemm(const void* A, const void* Wq, const void* scales, const
                         void* stream);
 
 /*
+ * Option bit OR-ed into w4a16_gemm_ex's `path` argument.
+ *
+ * W4A16_OPT_STATIC_WEIGHTS: the caller promises that Wq, scales and zeros are
+ * not written by any work that may still be running on the stream when this
+ * call's kernel starts (true for weights packed once and then only read).
+ * The kernels always start early behind the previous kernel on the stream
+ * (programmatic dependent launch) and wait for it before touching memory;
+ * with this bit the small-M kernel also fetches its weights during that wait,
+ * hiding HBM latency across back-to-back layers.  Activations and outputs are
+ * never touched before the previous kernel completes.
+ */
+#define W4A16_OPT_STATIC_WEIGHTS 0x100
+
+/*
  * w4a16_gemm_ex - w4a16_gemm with an optional dense copy and a path choice.
  * Wdense is NULL or a device dtype [N][K] dequantised copy (w4a16_dequant
  * output), 16-byte aligned; the prefill "cached dense-dequant" path of the
  * later rdna_hybrid_w4a16 revision (_cache_dequant_weight) uses it when the
- * router sends large M there.  path is a w4a16_path; forcing DECODE requires
- * M <= 64 and forcing DENSE requires Wdense (else W4A16_ERR_INVALID_ARG).
+ * router sends large M there.  path is a w4a16_path, optionally OR-ed with
+ * W4A16_OPT_STATIC_WEIGHTS; forcing DECODE requires M <= 64 and forcing DENSE
+ * requires Wdense (else W4A16_ERR_INVALID_ARG).
  */
 w4a16_status w4a16_gemm_ex(const void* A, const void* Wq, const void* scales,
                            const int32_t* zeros, const void* Wdense, void* C,

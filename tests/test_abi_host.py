@@ -41,6 +41,9 @@ def test_packed_layout_sizes(B):
     # K=48: K/8 = 6 words -> pitch 8; sections on 256-byte boundaries
     tot, so, zo, ldq = B.packed_layout(8, 48, -1, "uint4", "fp16")
     assert ldq == 8 and so == 256 and zo == 512 and tot == 768
+    # N=200: scale rows pad to 200 (already a multiple of 8), zero rows to 28 words
+    tot, so, zo, ldq = B.packed_layout(200, 1024, 64, "uint4", "fp16")
+    assert so == 200 * 128 * 4 and zo == so + 16 * 200 * 2 and tot == zo + 16 * 28 * 4
     tot, so, zo, ldq = B.packed_layout(11008, 4096, 32, "uint4", "bf16")
     assert so == 11008 * 512 * 4
     assert zo == so + 11008 * 128 * 2

@@ -25,7 +25,8 @@ SHAPES = [
     (32, 256, 1280, 256, "uint4", "bf16"),
     (64, 128, 512, -1, "uint4b8", "fp16"),
     (5, 64, 4112, -1, "uint4b8", "bf16"),      # K % 32 == 16
-    (1, 8, 16, -1, "uint4", "fp16"),           # smallest legal layer
+    (1, 8, 16, -1, "uint4", "fp16"),           # smallest legal layer (one group of 16)
+    (2, 16, 32, -1, "uint4", "bf16"),          # one group of 32
     (300, 384, 512, 128, "uint4b8", "bf16"),
     (77, 200, 1088, 64, "uint4", "fp16"),
     (40, 136, 4112, -1, "uint4b8", "bf16"),
@@ -55,12 +56,14 @@ def test_pack_is_bit_exact(cases, sh):
     w = DeviceWeight(p, x.q, x.scales, x.zeros)
     torch.cuda.synchronize()
     assert np.array_equal(w.words(), orc.pack_q(x.q, w.ldq))
-    # scale and zero sections are copies of the inputs
-    sc = to_host_bits(w.buf[w.so: w.so + p.N * p.ngroups * 2].view(TORCH[p.dtype]))
-    assert np.array_equal(sc.reshape(p.N, p.ngroups), x.scales)
+    # scale and zero sections are the inputs transposed, padded with zeros
+    lds, ldz = (p.N + 7) // 8 * 8, (p.N // 8 + 3) // 4 * 4
+    ng = p.ngroups
+    sc = to_host_bits(w.buf[w.so: w.so + ng * lds * 2].view(TORCH[p.dtype])).reshape(ng, lds)
+    assert np.array_equal(sc[:, :p.N], x.scales.T) and np.all(sc[:, p.N:] == 0)
     if x.zeros is not None:
-        z = w.buf[w.zo: w.zo + x.zeros.size * 4].view(torch.int32).cpu().numpy()
-        assert np.array_equal(z.reshape(x.zeros.shape), x.zeros)
+        z = w.buf[w.zo: w.zo + ng * ldz * 4].view(torch.int32).cpu().numpy().reshape(ng, ldz)
+        assert np.array_equal(z[:, :p.N // 8], x.zeros.T) and np.all(z[:, p.N // 8:] == 0)
     assert np.array_equal(orc.unpack_q(w.words(), p.K), x.q)
 
 

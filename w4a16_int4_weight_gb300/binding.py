@@ -22,6 +22,7 @@ PATH_AUTO, PATH_DECODE, PATH_FUSED, PATH_DENSE = range(4)
 QTYPES = {"uint4b8": UINT4B8, "uint4": UINT4}
 DTYPES = {"fp16": FP16, "bf16": BF16}
 PATHS = {"auto": PATH_AUTO, "decode": PATH_DECODE, "fused": PATH_FUSED, "dense": PATH_DENSE}
+OPT_STATIC_WEIGHTS = 0x100
 
 
 class W4A16Error(RuntimeError):
@@ -130,8 +131,10 @@ def gemm(A, Wq, scales, zeros, C, M, N, K, G, qtype, dtype, stream=None):
 
 
 def gemm_ex(A, Wq, scales, zeros, Wdense, C, M, N, K, G, qtype, dtype, path="auto",
-            stream=None):
+            stream=None, static_weights=False):
     p = PATHS[path] if isinstance(path, str) else int(path)
+    if static_weights:
+        p |= OPT_STATIC_WEIGHTS
     _check(lib.w4a16_gemm_ex(_ptr(A), _ptr(Wq), _ptr(scales), _ptr(zeros), _ptr(Wdense),
                              _ptr(C), M, N, K, G, _qt(qtype), _dt(dtype), p, _stream(stream)))
 

@@ -1,0 +1,391 @@
+// Small-M ("decode") W4A16 GEMM kernel: C[M,N] = A[M,K] . dequant(W)^T for M <= 64.
+//
+// The pages' skinny split-K decode kernel (wvSplitK_int4_g, called from
+// _rdna_hybrid_w4a16_apply_impl for M <= MAX_SKINNY_BATCH_SIZE) is only named
+// there; this is a GB300 design of the same job:
+//
+//  * Work split.  A CTA owns 128 weight rows and a contiguous run of 256-wide
+//    K boxes; the KS CTAs that share a row tile form one thread-block cluster
+//    and split K between them.  Their fp32 partials are pushed through
+//    distributed shared memory to the CTA that owns each row, so no global
+//    workspace and no atomics are used.
+//  * Data movement.  A producer warp streams, per K box and on one mbarrier,
+//    the packed weight box [128 rows x 32 words] (128-byte swizzle), the
+//    activation box [M x 256] as eight [M x 32] sub-boxes (64-byte swizzle,
+//    zero-filled past K) and the box's scales and zero points from the
+//    transposed scale / zero sections.  Consumer warps release a stage through
+//    a second mbarrier, so no CTA-wide barrier sits in the K loop.
+//  * Math.  Each consumer warp owns 16 rows.  A packed word (8 consecutive
+//    K-values of a row) is unpacked with one LOP3 per value pair into 16-bit
+//    floats (magic-number trick) and the zero point is subtracted exactly,
+//    giving the integers q - z; they are the A operand of mma.m16n8k16 (weights
+//    as MMA rows, tokens as MMA columns).  A thread's word covers 8 physical
+//    K-values and MMA step s uses values 4s..4s+3 of the words of a thread quad:
+//    a permutation of K applied to both operands, which leaves the dot product
+//    unchanged.  A quad's words span 32 consecutive K, inside one quantisation
+//    group (G >= 32), so the scale is applied once per group:
+//        C[n, m] = sum_g s[n,g] * sum_{k in g} A[m,k] (q[n,k] - z[n,g]).
+//    (The pages round each dequantised weight to the dtype before the dot; the
+//    result differs from this only by those roundings, well inside the output
+//    tolerance; w4a16_dequant keeps the exact per-weight rounding.)
+#pragma once
+
+#include <cooperative_groups.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace w4a16 {
+namespace decode {
+
+namespace cg = cooperative_groups;
+
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;   // + one producer warp
+constexpr int kBN = 16 * kConsumerWarps;               // weight rows per CTA
+constexpr int kBoxK = 256;               // K-values per box (32 words = 128 bytes per row)
+constexpr int kWBytes = kBN * 128;       // 16 KB packed weight box
+constexpr int kSubK = 32;                // K-values per activation sub-box (64 bytes per row)
+constexpr int kMaxStages = 4;
+constexpr int kMaxGps = 8;               // groups per box at G = 32
+
+struct Params {
+    uint16_t* C;
+    int* status;      // device status word (first timed-out wait site)
+    int M, N, K, g_eff;
+    int nboxes;       // ceil(K / kBoxK)
+    int ks;           // CTAs per cluster (K split)
+    int stages;       // ring depth (<= kMaxStages)
+    int gps;          // scale-tile rows per box
+    int a_slot;       // bytes of one [round_up(M,8) x 32] activation sub-box slot
+    int stage_bytes;  // bytes per stage (multiple of 1024)
+    int red_off;      // byte offset of the cluster reduction buffer
+    int prefetch_weights;   // weights may be read before the previous grid completes
+};
+
+struct StageView {
+    uint8_t* w;        // [128 rows][128 B], 128-byte swizzle
+    uint8_t* a;        // 8 x a_slot, each [rows][64 B], 64-byte swizzle
+    uint16_t* sc;      // [gps][128]
+    uint32_t* zp;      // [gps][16]
+};
+
+__device__ __forceinline__ StageView stage_view(uint8_t* base, const Params& p, int s) {
+    StageView v;
+    v.w = base + s * p.stage_bytes;
+    v.a = v.w + kWBytes;
+    v.sc = reinterpret_cast<uint16_t*>(v.a + 8 * p.a_slot);
+    v.zp = reinterpret_cast<uint32_t*>(v.sc + kMaxGps * kBN);
+    return v;
+}
+
+template <bool ZP>
+__device__ __forceinline__ void load_weights(const StageView& v, const CUtensorMap* tq,
+                                             const CUtensorMap* ts, const CUtensorMap* tz,
+                                             uint64_t* bar, int box, int n0, int g_eff) {
+    const int g0 = box * kBoxK / g_eff;
+    tma_load_2d(v.w, tq, bar, box * 32, n0);
+    tma_load_2d(v.sc, ts, bar, n0, g0);
+    if constexpr (ZP) tma_load_2d(v.zp, tz, bar, n0 / 8, g0);
+}
+
+__device__ __forceinline__ void load_acts(const StageView& v, const CUtensorMap* ta,
+                                          uint64_t* bar, int box, int a_slot) {
+#pragma unroll
+    for (int sub = 0; sub < kBoxK / kSubK; ++sub)
+        tma_load_2d(v.a + sub * a_slot, ta, bar, box * kBoxK + kSubK * sub, 0);
+}
+
+// WPG: 32-wide word steps per quantisation group (1, 2, 4 for G = 32, 64, 128);
+// 8 when a group spans whole boxes (G >= 256, or one group spanning K).
+template <int NT, bool BF16, bool ZP, int WPG>
+__global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                                                          const __grid_constant__ CUtensorMap tmap_a,
+                                                          const __grid_constant__ CUtensorMap tmap_s,
+                                                          const __grid_constant__ CUtensorMap tmap_z,
+                                                          const Params p) {
+    constexpr int MP = 8 * NT;                      // padded token count of the MMA column tiles
+    constexpr int NSETS = NT >= 4 ? 1 : 4 / NT;     // independent accumulator chains per tile
+    constexpr int GPB = 8 / WPG;                    // groups per box (1 in the large-group mode)
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.stages * p.stage_bytes);
+    uint64_t* empty = full + kMaxStages;
+    float* red = reinterpret_cast<float*>(smem + p.red_off);   // [ks][kBN/ks][MP]
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int rank = int(blockIdx.x) % p.ks;   // rank inside the cluster (cluster = (ks,1,1))
+    const int n0 = (int(blockIdx.x) / p.ks) * kBN;
+    const int b_lo = (rank * p.nboxes) / p.ks;
+    const int b_hi = ((rank + 1) * p.nboxes) / p.ks;
+    const int nb = b_hi - b_lo;
+    const int k_hi = min(p.K, b_hi * kBoxK);
+
+    if (tid == 0) {
+        for (int s = 0; s < kMaxStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsumerWarps);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    bool failed = false;
+    float acc[NT][4];
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[j][e] = 0.f;
+    const int g = lane >> 2, t = lane & 3;
+    const int r0 = warp * 16 + g, r1 = r0 + 8;   // rows within the tile; r % 8 == g
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------ producer ------------------------------
+        if (lane == 0) {
+            const uint32_t stage_tx = kWBytes + (kBoxK / kSubK) * uint32_t(p.M) * 64u +
+                                      uint32_t(p.gps) * kBN * 2u + (ZP ? uint32_t(p.gps) * 64u : 0u);
+            tma_prefetch_desc(&tmap_q);
+            tma_prefetch_desc(&tmap_a);
+            const int first = min(p.stages, nb);
+            // With static weights the packed weights, scales and zero points are
+            // requested before the previous grid in the stream has finished; the
+            // activations (and, without that promise, everything) only after it.
+            if (p.prefetch_weights) {
+                for (int i = 0; i < first; ++i) {
+                    mbar_arrive_expect_tx(&full[i], stage_tx);
+                    load_weights<ZP>(stage_view(smem, p, i), &tmap_q, &tmap_s, &tmap_z, &full[i],
+                                     b_lo + i, n0, p.g_eff);
+                }
+            }
+            grid_dependency_wait();
+            for (int i = 0; i < first; ++i) {
+                const StageView v = stage_view(smem, p, i);
+                if (!p.prefetch_weights) {
+                    mbar_arrive_expect_tx(&full[i], stage_tx);
+                    load_weights<ZP>(v, &tmap_q, &tmap_s, &tmap_z, &full[i], b_lo + i, n0, p.g_eff);
+                }
+                load_acts(v, &tmap_a, &full[i], b_lo + i, p.a_slot);
+            }
+            // the next kernel in the stream may start its own prologue now
+            grid_launch_dependents();
+            int issued = first;
+            for (; issued < nb; ++issued) {
+                const int s = issued % p.stages;
+                if (!mbar_wait(&empty[s], uint32_t(issued / p.stages - 1) & 1u, p.status, 3)) break;
+                const StageView v = stage_view(smem, p, s);
+                mbar_arrive_expect_tx(&full[s], stage_tx);
+                load_weights<ZP>(v, &tmap_q, &tmap_s, &tmap_z, &full[s], b_lo + issued, n0, p.g_eff);
+                load_acts(v, &tmap_a, &full[s], b_lo + issued, p.a_slot);
+            }
+            // copies still in flight must land before the CTA retires
+            for (int i = max(0, issued - p.stages); i < issued; ++i)
+                mbar_wait(&full[i % p.stages], uint32_t(i / p.stages) & 1u, p.status, 2);
+        }
+    } else {
+        // ------------------------------ consumers -----------------------------
+        float accg[NSETS][NT][4];
+#pragma unroll
+        for (int c = 0; c < NSETS; ++c)
+#pragma unroll
+            for (int j = 0; j < NT; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) accg[c][j][e] = 0.f;
+        float s0 = 0.f, s1 = 0.f;
+        ZeroConst zc0 = make_zero_const<BF16>(8), zc1 = zc0;
+        int cur_g = -1;   // large-group mode: group whose sums accg holds
+
+        auto flush = [&]() {
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                float v[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    v[e] = accg[0][j][e];
+#pragma unroll
+                    for (int c = 1; c < NSETS; ++c) v[e] += accg[c][j][e];
+#pragma unroll
+                    for (int c = 0; c < NSETS; ++c) accg[c][j][e] = 0.f;
+                }
+                acc[j][0] = fmaf(s0, v[0], acc[j][0]);
+                acc[j][1] = fmaf(s0, v[1], acc[j][1]);
+                acc[j][2] = fmaf(s1, v[2], acc[j][2]);
+                acc[j][3] = fmaf(s1, v[3], acc[j][3]);
+            }
+        };
+        auto load_group = [&](const StageView& v, int gl) {
+            s0 = to_f32<BF16>(v.sc[gl * kBN + r0]);
+            s1 = to_f32<BF16>(v.sc[gl * kBN + r1]);
+            if constexpr (ZP) {
+                zc0 = make_zero_const<BF16>((v.zp[gl * 16 + (r0 >> 3)] >> (4 * g)) & 0xF);
+                zc1 = make_zero_const<BF16>((v.zp[gl * 16 + (r1 >> 3)] >> (4 * g)) & 0xF);
+            }
+        };
+        // per-thread shared-memory offsets that do not depend on the stage
+        const int wrow0 = r0 * 128 + (t << 2), wrow1 = r1 * 128 + (t << 2);
+        int aoff[NT];
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+            const int tok = 8 * j + g;
+            aoff[j] = tok * 64 + ((t ^ ((tok >> 1) & 3)) << 4);
+        }
+
+        for (int i = 0; i < nb; ++i) {
+            const int stage = i % p.stages;
+            const bool got = __all_sync(0xffffffffu,
+                                        mbar_wait(&full[stage], uint32_t(i / p.stages) & 1u, p.status, 1));
+            if (!got) { failed = true; break; }
+            const StageView v = stage_view(smem, p, stage);
+            const int box_k = (b_lo + i) * kBoxK;
+            if constexpr (WPG == 8) {
+                const int grp = box_k / p.g_eff;
+                if (grp != cur_g) {
+                    if (cur_g >= 0) flush();
+                    cur_g = grp;
+                    load_group(v, 0);
+                }
+            }
+#pragma unroll
+            for (int gi = 0; gi < GPB; ++gi) {
+                const int kw0 = box_k + gi * WPG * 32;
+                if (kw0 >= k_hi) break;
+                if constexpr (WPG < 8) load_group(v, gi);
+#pragma unroll
+                for (int w = 0; w < WPG; ++w) {
+                    const int ws = gi * WPG + w;
+                    if (kw0 + w * 32 >= k_hi) break;
+                    // word ws*4 + t of the box row: 16-byte chunk ws sits at chunk ws ^ (row % 8)
+                    const int woff = (ws ^ g) << 4;
+                    const uint32_t w0 = *reinterpret_cast<const uint32_t*>(v.w + wrow0 + woff);
+                    const uint32_t w1 = *reinterpret_cast<const uint32_t*>(v.w + wrow1 + woff);
+                    uint32_t q0[4], q1[4];
+                    unpack_word<BF16>(w0, zc0, q0);
+                    unpack_word<BF16>(w1, zc1, q1);
+                    const uint32_t a_s0[4] = {q0[0], q1[0], q0[1], q1[1]};
+                    const uint32_t a_s1[4] = {q0[2], q1[2], q0[3], q1[3]};
+                    // activation K-values kw + 8t .. +7: sub-box ws, 16-byte chunk t, which
+                    // the 64-byte swizzle places at chunk t ^ ((row / 2) % 4)
+                    const uint8_t* abox = v.a + ws * p.a_slot;
+#pragma unroll
+                    for (int j = 0; j < NT; ++j) {
+                        uint4 b = make_uint4(0u, 0u, 0u, 0u);
+                        if (8 * j + g < p.M) b = *reinterpret_cast<const uint4*>(abox + aoff[j]);
+                        mma_m16n8k16<BF16>(accg[(2 * ws) % NSETS][j], a_s0, b.x, b.y);
+                        mma_m16n8k16<BF16>(accg[(2 * ws + 1) % NSETS][j], a_s1, b.z, b.w);
+                    }
+                }
+                if constexpr (WPG < 8) flush();
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[stage]);
+        }
+        if constexpr (WPG == 8) {
+            if (cur_g >= 0) flush();
+        }
+    }
+
+    // C fragment: (row g, tokens 2t, 2t+1) and (row g + 8, same tokens)
+    const bool consumer = warp < kConsumerWarps;
+    if (p.ks == 1) {
+        if (consumer && !failed) {
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int tok = 8 * j + 2 * t + (e & 1);
+                    const int n = n0 + (e < 2 ? r0 : r1);
+                    if (tok < p.M && n < p.N) p.C[size_t(tok) * p.N + n] = from_f32<BF16>(acc[j][e]);
+                }
+            }
+        }
+        __syncthreads();   // the producer's final waits end before the CTA retires
+        return;
+    }
+    // Split K: push each partial to the CTA that owns its row, into slot `rank`
+    // of that CTA's reduction buffer, then one cluster barrier.
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rows_per = kBN / p.ks;
+    if (consumer) {
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int tok = 8 * j + 2 * t + (e & 1);
+                const int row = e < 2 ? r0 : r1;
+                const int owner = row / rows_per;
+                float* dst = cluster.map_shared_rank(red, owner);
+                dst[(rank * rows_per + (row - owner * rows_per)) * MP + tok] = acc[j][e];
+            }
+        }
+    }
+    const int any_failed = __syncthreads_or(failed);
+    cluster.sync();
+    const int items = rows_per * p.M;
+    for (int it = tid; it < items; it += kThreads) {
+        const int rl = it % rows_per, tok = it / rows_per;
+        float sum = 0.f;
+        for (int c = 0; c < p.ks; ++c) sum += red[(c * rows_per + rl) * MP + tok];
+        const int n = n0 + rank * rows_per + rl;
+        if (n < p.N && !any_failed) p.C[size_t(tok) * p.N + n] = from_f32<BF16>(sum);
+    }
+}
+
+template <int NT, bool BF16, bool ZP, int WPG>
+cudaError_t launch_one(const CUtensorMap* maps, const Params& p, int grid, size_t smem,
+                       cudaStream_t stream) {
+    auto kern = decode_kernel<NT, BF16, ZP, WPG>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = p.ks;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], p);
+}
+
+template <bool BF16, bool ZP, int WPG>
+cudaError_t launch_nt(int nt, const CUtensorMap* maps, const Params& p, int grid, size_t smem,
+                      cudaStream_t stream) {
+    switch (nt) {
+        case 1: return launch_one<1, BF16, ZP, WPG>(maps, p, grid, smem, stream);
+        case 2: return launch_one<2, BF16, ZP, WPG>(maps, p, grid, smem, stream);
+        case 4: return launch_one<4, BF16, ZP, WPG>(maps, p, grid, smem, stream);
+        default: return launch_one<8, BF16, ZP, WPG>(maps, p, grid, smem, stream);
+    }
+}
+
+template <bool BF16>
+cudaError_t launch_dtype(bool zp, int wpg, int nt, const CUtensorMap* maps, const Params& p,
+                         int grid, size_t smem, cudaStream_t stream) {
+#define W4A16_DECODE_WPG(W)                                                                       \
+    case W:                                                                                      \
+        return zp ? launch_nt<BF16, true, W>(nt, maps, p, grid, smem, stream)                   \
+                  : launch_nt<BF16, false, W>(nt, maps, p, grid, smem, stream);
+    switch (wpg) {
+        W4A16_DECODE_WPG(1)
+        W4A16_DECODE_WPG(2)
+        W4A16_DECODE_WPG(4)
+        W4A16_DECODE_WPG(8)
+        default: return cudaErrorInvalidValue;
+    }
+#undef W4A16_DECODE_WPG
+}
+
+// Defined in decode_bf16.cu / decode_fp16.cu (one dtype per translation unit).
+cudaError_t launch_bf16(bool zp, int wpg, int nt, const CUtensorMap* maps, const Params& p,
+                        int grid, size_t smem, cudaStream_t stream);
+cudaError_t launch_fp16(bool zp, int wpg, int nt, const CUtensorMap* maps, const Params& p,
+                        int grid, size_t smem, cudaStream_t stream);
+
+}  // namespace decode
+}  // namespace w4a16

@@ -13,6 +13,8 @@ struct LayerShape {
     int64_t g_eff;   // group size with -1 resolved to K
     int64_t ng;      // K / g_eff
     int64_t ldq;     // packed row pitch in 32-bit words
+    int64_t lds;     // transposed scale row pitch in elements: round_up(N, 8)
+    int64_t ldz;     // transposed zero-point row pitch in words: round_up(N/8, 4)
     bool bf16;       // activation dtype
     bool zp;         // explicit zero points (uint4)
 };
@@ -26,15 +28,21 @@ cudaError_t launch_dequant(const uint32_t* Wq, const void* scales, const int32_t
 
 // decode.cu: small-M split-K kernel, M <= kDecodeMaxM.
 constexpr int64_t kDecodeMaxM = 64;
-cudaError_t launch_decode(const CUtensorMap& tmap_q, const void* A, const void* scales,
-                          const int32_t* zeros, void* C, const LayerShape& s,
-                          int num_sms, cudaStream_t stream);
+// maps: packed q [N][ldq] u32 box {32,128} SW128; A [M][K] box {32,M} SW64;
+// scales [ng][lds] box {128, decode_scale_box_rows}; zeros [ng][ldz] box {16, same}.
+// prefetch_weights: the weights are not written by work still running on the
+// stream, so they may be fetched before the previous grid completes.
+cudaError_t launch_decode(const CUtensorMap* maps, void* C, const LayerShape& s, int num_sms,
+                          bool prefetch_weights, cudaStream_t stream);
+int decode_scale_box_rows(int64_t g_eff, int64_t ng);
+bool plan_decode(int64_t M, int64_t N, int64_t K, int num_sms, int* ks_out, int* stages_out,
+                 size_t* smem_out, int* nt_out);
 
 // prefill.cu: tcgen05 GEMM, fused-dequant (Wq != null) or dense (tmap_w dense).
-cudaError_t launch_prefill(const CUtensorMap& tmap_a, const CUtensorMap& tmap_w,
-                           const void* scales, const int32_t* zeros, void* C,
-                           const LayerShape& s, bool dense, int token_tile,
-                           cudaStream_t stream);
+// maps: A [M][K] box {64,BT} SW128; weights (packed [N][ldq] box {8,128}, or
+// dense [N][K] box {64,128} SW128); scales [ng][lds] box {128,2}; zeros [ng][ldz] box {16,2}.
+cudaError_t launch_prefill(const CUtensorMap* maps, void* C, const LayerShape& s, bool dense,
+                           int token_tile, cudaStream_t stream);
 
 // Status words of each module: read-and-clear (synchronous).
 int take_status_decode();

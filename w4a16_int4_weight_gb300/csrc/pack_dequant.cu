@@ -38,19 +38,27 @@ __global__ void __launch_bounds__(kThreads) pack_q_kernel(const uint8_t* __restr
     }
 }
 
+// [rows][cols] (row-major) -> [cols][ld] with zero padding for r >= rows.  The
+// output is written in full and in order (coalesced); the strided reads touch
+// each input element once.  Scales and zero points are a small fraction of the
+// weight, and this runs once per weight.
 template <typename T>
-__global__ void __launch_bounds__(kThreads) copy_kernel(const T* __restrict__ src,
-                                                        T* __restrict__ dst, int64_t count) {
-    for (int64_t i = int64_t(blockIdx.x) * kThreads + threadIdx.x; i < count;
-         i += int64_t(gridDim.x) * kThreads)
-        dst[i] = src[i];
+__global__ void __launch_bounds__(kThreads) transpose_pad_kernel(const T* __restrict__ src,
+                                                                 T* __restrict__ dst, int64_t rows,
+                                                                 int64_t cols, int64_t ld) {
+    const int64_t total = cols * ld;
+    for (int64_t i = int64_t(blockIdx.x) * kThreads + threadIdx.x; i < total;
+         i += int64_t(gridDim.x) * kThreads) {
+        const int64_t c = i / ld, r = i % ld;
+        dst[i] = r < rows ? src[r * cols + c] : T(0);
+    }
 }
 
 template <bool BF16, bool ZP>
 __global__ void __launch_bounds__(kThreads) dequant_kernel(
     const uint32_t* __restrict__ wq, const uint16_t* __restrict__ scales,
     const int32_t* __restrict__ zeros, uint16_t* __restrict__ out, int64_t N, int64_t K,
-    int64_t ldq, int64_t g_eff, int64_t ng) {
+    int64_t ldq, int64_t g_eff, int64_t lds, int64_t ldz) {
     const int64_t k8 = K / 8, l4 = (k8 + 3) / 4, total = N * l4;
     for (int64_t i = int64_t(blockIdx.x) * kThreads + threadIdx.x; i < total;
          i += int64_t(gridDim.x) * kThreads) {
@@ -62,9 +70,9 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(
             const int64_t j = j0 + t;
             if (j >= k8) break;
             const int64_t g = (8 * j) / g_eff;   // g_eff is a multiple of 8: one group per word
-            const uint16_t sb = __ldg(scales + n * ng + g);
+            const uint16_t sb = __ldg(scales + g * lds + n);
             int z = 8;
-            if constexpr (ZP) z = (__ldg(zeros + (n / 8) * ng + g) >> (4 * (n % 8))) & 0xF;
+            if constexpr (ZP) z = (__ldg(zeros + g * ldz + n / 8) >> (4 * (n % 8))) & 0xF;
             const uint32_t s2 = uint32_t(sb) | (uint32_t(sb) << 16);
             uint32_t p[4];
             unpack_word<BF16>(wv[t], make_zero_const<BF16>(z), p);
@@ -94,20 +102,13 @@ cudaError_t launch_pack(const uint8_t* q, const void* scales, const int32_t* zer
                                                              s.K, s.ldq);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    if (scales_dst != scales) {
-        const int64_t cnt = s.N * s.ng;
-        copy_kernel<uint16_t><<<grid_for(cnt), kThreads, 0, stream>>>(
-            static_cast<const uint16_t*>(scales), static_cast<uint16_t*>(scales_dst), cnt);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-    }
-    if (s.zp && zeros_dst != zeros) {
-        const int64_t cnt = (s.N / 8) * s.ng;
-        copy_kernel<int32_t><<<grid_for(cnt), kThreads, 0, stream>>>(
-            zeros, static_cast<int32_t*>(zeros_dst), cnt);
-        e = cudaGetLastError();
-    }
-    return e;
+    transpose_pad_kernel<uint16_t><<<grid_for(s.ng * s.lds), kThreads, 0, stream>>>(
+        static_cast<const uint16_t*>(scales), static_cast<uint16_t*>(scales_dst), s.N, s.ng, s.lds);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || !s.zp) return e;
+    transpose_pad_kernel<int32_t><<<grid_for(s.ng * s.ldz), kThreads, 0, stream>>>(
+        zeros, static_cast<int32_t*>(zeros_dst), s.N / 8, s.ng, s.ldz);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_dequant(const uint32_t* Wq, const void* scales, const int32_t* zeros,
@@ -117,11 +118,11 @@ cudaError_t launch_dequant(const uint32_t* Wq, const void* scales, const int32_t
     auto* out = static_cast<uint16_t*>(W);
     const int grid = grid_for(items);
     if (s.bf16) {
-        if (s.zp) dequant_kernel<true, true><<<grid, kThreads, 0, stream>>>(Wq, sc, zeros, out, s.N, s.K, s.ldq, s.g_eff, s.ng);
-        else dequant_kernel<true, false><<<grid, kThreads, 0, stream>>>(Wq, sc, zeros, out, s.N, s.K, s.ldq, s.g_eff, s.ng);
+        if (s.zp) dequant_kernel<true, true><<<grid, kThreads, 0, stream>>>(Wq, sc, zeros, out, s.N, s.K, s.ldq, s.g_eff, s.lds, s.ldz);
+        else dequant_kernel<true, false><<<grid, kThreads, 0, stream>>>(Wq, sc, zeros, out, s.N, s.K, s.ldq, s.g_eff, s.lds, s.ldz);
     } else {
-        if (s.zp) dequant_kernel<false, true><<<grid, kThreads, 0, stream>>>(Wq, sc, zeros, out, s.N, s.K, s.ldq, s.g_eff, s.ng);
-        else dequant_kernel<false, false><<<grid, kThreads, 0, stream>>>(Wq, sc, zeros, out, s.N, s.K, s.ldq, s.g_eff, s.ng);
+        if (s.zp) dequant_kernel<false, true><<<grid, kThreads, 0, stream>>>(Wq, sc, zeros, out, s.N, s.K, s.ldq, s.g_eff, s.lds, s.ldz);
+        else dequant_kernel<false, false><<<grid, kThreads, 0, stream>>>(Wq, sc, zeros, out, s.N, s.K, s.ldq, s.g_eff, s.lds, s.ldz);
     }
     return cudaGetLastError();
 }

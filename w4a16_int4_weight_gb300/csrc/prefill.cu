@@ -33,12 +33,12 @@ constexpr int kStages = 4;
 constexpr int kThreads = 192;
 constexpr int kWtBytes = kBM * 128;       // 16 KB dequantised / dense weight tile
 constexpr int kPkBytes = kBM * 32;        // 4 KB packed tile (8 words per row)
+constexpr int kScBytes = 2 * kBM * 2;     // scales of two groups x 128 rows
+constexpr int kZpBytes = 2 * 16 * 4;      // zero-point words of two groups x 128 rows
 
 __device__ int g_status;
 
 struct Params {
-    const uint16_t* scales;
-    const int32_t* zeros;
     uint16_t* C;
     int M, N, K, g_eff, ng;
     int nkb;   // ceil(K / kBK)
@@ -47,7 +47,8 @@ struct Params {
 template <int BT, bool DENSE>
 struct Layout {
     static constexpr int kActBytes = BT * 128;
-    static constexpr int kStageBytes = kActBytes + kWtBytes + (DENSE ? 0 : kPkBytes);
+    static constexpr int kStageBytes =
+        (kActBytes + kWtBytes + (DENSE ? 0 : kPkBytes + kScBytes + kZpBytes) + 1023) / 1024 * 1024;
     static constexpr int kBarOff = kStages * kStageBytes;
     static constexpr int kBytes = kBarOff + 256 + 1024;   // + barriers, + alignment slack
 };
@@ -55,6 +56,8 @@ struct Layout {
 template <bool BF16, bool ZP, int BT, bool DENSE>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                                               const __grid_constant__ CUtensorMap tmap_w,
+                                                              const __grid_constant__ CUtensorMap tmap_s,
+                                                              const __grid_constant__ CUtensorMap tmap_z,
                                                               const Params p) {
     using L = Layout<BT, DENSE>;
     extern __shared__ uint8_t smem_raw[];
@@ -63,6 +66,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     auto act_tile = [&](int s) { return smem + s * L::kStageBytes; };
     auto wt_tile = [&](int s) { return smem + s * L::kStageBytes + L::kActBytes; };
     auto pk_tile = [&](int s) { return smem + s * L::kStageBytes + L::kActBytes + kWtBytes; };
+    auto sc_tile = [&](int s) {   // [2 groups][128 rows] of dtype bits
+        return reinterpret_cast<uint16_t*>(pk_tile(s) + kPkBytes);
+    };
+    auto zp_tile = [&](int s) {   // [2 groups][16 words]
+        return reinterpret_cast<uint32_t*>(pk_tile(s) + kPkBytes + kScBytes);
+    };
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
     uint64_t* dq_full = full + kStages;
     uint64_t* empty = dq_full + kStages;
@@ -104,10 +113,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 if (kb >= kStages)
                     ok = mbar_wait(&empty[s], uint32_t(kb / kStages - 1) & 1u, &g_status, 10);
                 if (!ok) break;
-                mbar_arrive_expect_tx(&full[s], L::kActBytes + (DENSE ? kWtBytes : kPkBytes));
+                mbar_arrive_expect_tx(&full[s], L::kActBytes + (DENSE ? kWtBytes
+                                                     : kPkBytes + kScBytes + (ZP ? kZpBytes : 0)));
                 tma_load_2d(act_tile(s), &tmap_a, &full[s], kb * kBK, m0);
-                if constexpr (DENSE) tma_load_2d(wt_tile(s), &tmap_w, &full[s], kb * kBK, n0);
-                else tma_load_2d(pk_tile(s), &tmap_w, &full[s], kb * (kBK / 8), n0);
+                if constexpr (DENSE) {
+                    tma_load_2d(wt_tile(s), &tmap_w, &full[s], kb * kBK, n0);
+                } else {
+                    // the K block's first group and the one after it (used when G = 32)
+                    const int g0 = (kb * kBK) / p.g_eff;
+                    tma_load_2d(pk_tile(s), &tmap_w, &full[s], kb * (kBK / 8), n0);
+                    tma_load_2d(sc_tile(s), &tmap_s, &full[s], n0, g0);
+                    if constexpr (ZP) tma_load_2d(zp_tile(s), &tmap_z, &full[s], n0 / 8, g0);
+                }
                 ++issued;
             }
             // copies still in flight must land before the CTA can retire
@@ -139,7 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         // ---------------- dequantisers (warps 0-3), then epilogue ----------------
         const int row = tid;                 // weight row within the tile
         const int n = n0 + row;
-        const bool row_ok = n < p.N;
+        const bool row_ok = n < p.N;        // rows past N read zero-filled tiles
         bool ok = true;
         if constexpr (!DENSE) {
             for (int kb = 0; kb < p.nkb; ++kb) {
@@ -151,21 +168,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 const uint4 wa = src[0], wb = src[1];
                 const uint32_t words[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
                 // words 0-3 (K-values kb*64 + 0..31) and 4-7 (+32..63) each lie in one
-                // group because every group size is a multiple of 32
-                const int k0 = kb * kBK;
-                const int ga = min(k0 / p.g_eff, p.ng - 1);
-                const int gb = min((k0 + 32) / p.g_eff, p.ng - 1);
-                uint32_t s2a = 0, s2b = 0;
+                // group: every group size is a multiple of 32, or there is one group.
+                // The second half uses the tile's second group row only when G = 32.
+                const int gb = (p.g_eff == 32 && p.ng > 1) ? 1 : 0;
+                const uint16_t* sc = sc_tile(s);
+                const uint32_t sa = sc[row], sb = sc[gb * kBM + row];
+                const uint32_t s2a = sa | (sa << 16), s2b = sb | (sb << 16);
                 int za = 8, zb = 8;
-                if (row_ok) {
-                    const uint32_t sa = __ldg(p.scales + size_t(n) * p.ng + ga);
-                    const uint32_t sb = __ldg(p.scales + size_t(n) * p.ng + gb);
-                    s2a = sa | (sa << 16);
-                    s2b = sb | (sb << 16);
-                    if constexpr (ZP) {
-                        za = (__ldg(p.zeros + size_t(n >> 3) * p.ng + ga) >> (4 * (n & 7))) & 0xF;
-                        zb = (__ldg(p.zeros + size_t(n >> 3) * p.ng + gb) >> (4 * (n & 7))) & 0xF;
-                    }
+                if constexpr (ZP) {
+                    const uint32_t* zt = zp_tile(s);
+                    za = (zt[row >> 3] >> (4 * (row & 7))) & 0xF;
+                    zb = (zt[gb * 16 + (row >> 3)] >> (4 * (row & 7))) & 0xF;
                 }
                 const ZeroConst zca = make_zero_const<BF16>(za);
                 const ZeroConst zcb = make_zero_const<BF16>(zb);
@@ -216,37 +229,32 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 }
 
 template <bool BF16, bool ZP, int BT, bool DENSE>
-cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tw, const Params& p,
-                     cudaStream_t stream) {
+cudaError_t launch_t(const CUtensorMap* maps, const Params& p, cudaStream_t stream) {
     auto kern = prefill_kernel<BF16, ZP, BT, DENSE>;
     constexpr int smem = Layout<BT, DENSE>::kBytes;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     dim3 grid((p.N + kBM - 1) / kBM, (p.M + BT - 1) / BT);
-    kern<<<grid, kThreads, smem, stream>>>(ta, tw, p);
+    kern<<<grid, kThreads, smem, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
     return cudaGetLastError();
 }
 
 template <int BT>
-cudaError_t launch_bt(const CUtensorMap& ta, const CUtensorMap& tw, const Params& p, bool bf16,
-                      bool zp, bool dense, cudaStream_t stream) {
-    if (dense) return bf16 ? launch_t<true, false, BT, true>(ta, tw, p, stream)
-                           : launch_t<false, false, BT, true>(ta, tw, p, stream);
-    if (bf16) return zp ? launch_t<true, true, BT, false>(ta, tw, p, stream)
-                        : launch_t<true, false, BT, false>(ta, tw, p, stream);
-    return zp ? launch_t<false, true, BT, false>(ta, tw, p, stream)
-              : launch_t<false, false, BT, false>(ta, tw, p, stream);
+cudaError_t launch_bt(const CUtensorMap* maps, const Params& p, bool bf16, bool zp, bool dense,
+                      cudaStream_t stream) {
+    if (dense) return bf16 ? launch_t<true, false, BT, true>(maps, p, stream)
+                           : launch_t<false, false, BT, true>(maps, p, stream);
+    if (bf16) return zp ? launch_t<true, true, BT, false>(maps, p, stream)
+                        : launch_t<true, false, BT, false>(maps, p, stream);
+    return zp ? launch_t<false, true, BT, false>(maps, p, stream)
+              : launch_t<false, false, BT, false>(maps, p, stream);
 }
 
 }  // namespace
 
-cudaError_t launch_prefill(const CUtensorMap& tmap_a, const CUtensorMap& tmap_w,
-                           const void* scales, const int32_t* zeros, void* C,
-                           const LayerShape& s, bool dense, int token_tile,
-                           cudaStream_t stream) {
+cudaError_t launch_prefill(const CUtensorMap* maps, void* C, const LayerShape& s, bool dense,
+                           int token_tile, cudaStream_t stream) {
     Params p;
-    p.scales = static_cast<const uint16_t*>(scales);
-    p.zeros = zeros;
     p.C = static_cast<uint16_t*>(C);
     p.M = int(s.M);
     p.N = int(s.N);
@@ -255,9 +263,9 @@ cudaError_t launch_prefill(const CUtensorMap& tmap_a, const CUtensorMap& tmap_w,
     p.ng = int(s.ng);
     p.nkb = int((s.K + kBK - 1) / kBK);
     switch (token_tile) {
-        case 64: return launch_bt<64>(tmap_a, tmap_w, p, s.bf16, s.zp, dense, stream);
-        case 128: return launch_bt<128>(tmap_a, tmap_w, p, s.bf16, s.zp, dense, stream);
-        default: return launch_bt<256>(tmap_a, tmap_w, p, s.bf16, s.zp, dense, stream);
+        case 64: return launch_bt<64>(maps, p, s.bf16, s.zp, dense, stream);
+        case 128: return launch_bt<128>(maps, p, s.bf16, s.zp, dense, stream);
+        default: return launch_bt<256>(maps, p, s.bf16, s.zp, dense, stream);
     }
 }
 

@@ -11,13 +11,8 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/w4a16.h"
+#include "w4a16.h"
 #include "internal.h"
-
-namespace w4a16 {
-bool plan_decode(int64_t M, int64_t N, int64_t K, int num_sms, int* ks_out, int* stages_out,
-                 size_t* smem_out, int* nt_out);
-}
 
 namespace {
 
@@ -65,6 +60,8 @@ w4a16_status check_weight(int64_t N, int64_t K, int G, int qtype, int dtype, Lay
         s->g_eff = g_eff;
         s->ng = K / g_eff;
         s->ldq = (K / 8 + 3) / 4 * 4;
+        s->lds = (N + 7) / 8 * 8;
+        s->ldz = (N / 8 + 3) / 4 * 4;
         s->bf16 = dtype == W4A16_BF16;
         s->zp = qtype == W4A16_UINT4;
         s->M = 0;
@@ -74,9 +71,9 @@ w4a16_status check_weight(int64_t N, int64_t K, int G, int qtype, int dtype, Lay
 
 w4a16_status check_qptrs(const void* Wq, const void* scales, const int32_t* zeros, int qtype) {
     if (!Wq || !aligned(Wq, 16)) return fail(W4A16_ERR_INVALID_ARG, "Wq must be a non-null 16-byte aligned device pointer");
-    if (!scales || !aligned(scales, 2)) return fail(W4A16_ERR_INVALID_ARG, "scales must be a non-null 2-byte aligned device pointer");
+    if (!scales || !aligned(scales, 16)) return fail(W4A16_ERR_INVALID_ARG, "scales must be a non-null 16-byte aligned device pointer (the packed scale section)");
     if (qtype == W4A16_UINT4) {
-        if (!zeros || !aligned(zeros, 4)) return fail(W4A16_ERR_INVALID_ARG, "uint4 needs a non-null 4-byte aligned zeros pointer");
+        if (!zeros || !aligned(zeros, 16)) return fail(W4A16_ERR_INVALID_ARG, "uint4 needs a non-null 16-byte aligned zeros pointer (the packed zero section)");
     } else if (zeros) {
         return fail(W4A16_ERR_INVALID_ARG, "zeros must be NULL for uint4b8 (the zero point is the constant 8)");
     }
@@ -170,34 +167,62 @@ w4a16_status launch_tcgen05(const void* A, const void* Wsrc, bool dense, const v
                             const int32_t* zeros, void* C, const LayerShape& s,
                             cudaStream_t stream) {
     const int bt = token_tile_for(s.M);
-    CUtensorMap ta, tw;
-    w4a16_status st = make_map(&ta, A, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, uint64_t(s.K),
+    CUtensorMap maps[4];
+    w4a16_status st = make_map(&maps[0], A, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, uint64_t(s.K),
                                uint64_t(s.M), uint64_t(s.K) * 2, 64, uint32_t(bt),
                                CU_TENSOR_MAP_SWIZZLE_128B);
     if (st) return st;
-    if (dense)
-        st = make_map(&tw, Wsrc, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, uint64_t(s.K), uint64_t(s.N),
+    if (dense) {
+        st = make_map(&maps[1], Wsrc, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, uint64_t(s.K), uint64_t(s.N),
                       uint64_t(s.K) * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
-    else
-        st = make_map(&tw, Wsrc, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, uint64_t(s.ldq), uint64_t(s.N),
+        if (st) return st;
+        maps[2] = maps[0];   // unused by the dense kernel
+        maps[3] = maps[0];
+    } else {
+        st = make_map(&maps[1], Wsrc, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, uint64_t(s.ldq), uint64_t(s.N),
                       uint64_t(s.ldq) * 4, 8, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
-    if (st) return st;
-    cudaError_t e = launch_prefill(ta, tw, scales, zeros, C, s, dense, bt, stream);
+        if (st) return st;
+        st = make_map(&maps[2], scales, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, uint64_t(s.lds),
+                      uint64_t(s.ng), uint64_t(s.lds) * 2, 128, 2, CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (st) return st;
+        if (s.zp) {
+            st = make_map(&maps[3], zeros, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, uint64_t(s.ldz),
+                          uint64_t(s.ng), uint64_t(s.ldz) * 4, 16, 2, CU_TENSOR_MAP_SWIZZLE_NONE);
+            if (st) return st;
+        } else {
+            maps[3] = maps[2];   // unused without zero points
+        }
+    }
+    cudaError_t e = launch_prefill(maps, C, s, dense, bt, stream);
     if (e != cudaSuccess) return cuda_fail(e, "tcgen05 GEMM launch");
     return W4A16_OK;
 }
 
 w4a16_status launch_decode_path(const void* A, const void* Wq, const void* scales,
                                 const int32_t* zeros, void* C, const LayerShape& s,
-                                cudaStream_t stream) {
+                                bool static_weights, cudaStream_t stream) {
     int sms = 0;
     w4a16_status st = device_sms(&sms);
     if (st) return st;
-    CUtensorMap tq;
-    st = make_map(&tq, Wq, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, uint64_t(s.ldq), uint64_t(s.N),
+    const uint32_t gps = uint32_t(decode_scale_box_rows(s.g_eff, s.ng));
+    CUtensorMap maps[4];
+    st = make_map(&maps[0], Wq, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, uint64_t(s.ldq), uint64_t(s.N),
                   uint64_t(s.ldq) * 4, 32, 128, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st) return st;
-    cudaError_t e = launch_decode(tq, A, scales, zeros, C, s, sms, stream);
+    st = make_map(&maps[1], A, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, uint64_t(s.K), uint64_t(s.M),
+                  uint64_t(s.K) * 2, 32, uint32_t(s.M), CU_TENSOR_MAP_SWIZZLE_64B);
+    if (st) return st;
+    st = make_map(&maps[2], scales, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, uint64_t(s.lds), uint64_t(s.ng),
+                  uint64_t(s.lds) * 2, 128, gps, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (st) return st;
+    if (s.zp) {
+        st = make_map(&maps[3], zeros, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, uint64_t(s.ldz), uint64_t(s.ng),
+                      uint64_t(s.ldz) * 4, 16, gps, CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (st) return st;
+    } else {
+        maps[3] = maps[2];   // unused without zero points
+    }
+    cudaError_t e = launch_decode(maps, C, s, sms, static_weights, stream);
     if (e != cudaSuccess) return cuda_fail(e, "decode GEMM launch");
     return W4A16_OK;
 }
@@ -218,11 +243,11 @@ w4a16_status w4a16_packed_layout(int64_t N, int64_t K, int G, int qtype, int dty
     if (st) return st;
     const size_t q_bytes = size_t(N) * size_t(s.ldq) * 4;
     const size_t so = round_up(q_bytes, 256);
-    const size_t s_bytes = size_t(N) * size_t(s.ng) * 2;
+    const size_t s_bytes = size_t(s.ng) * size_t(s.lds) * 2;
     size_t zo = 0, end = so + s_bytes;
     if (s.zp) {
         zo = round_up(end, 256);
-        end = zo + size_t(N / 8) * size_t(s.ng) * 4;
+        end = zo + size_t(s.ng) * size_t(s.ldz) * 4;
     }
     if (total_bytes) *total_bytes = round_up(end, 256);
     if (scales_off) *scales_off = so;
@@ -266,6 +291,9 @@ w4a16_status w4a16_gemm_ex(const void* A, const void* Wq, const void* scales,
     w4a16_status st = check_weight(N, K, G, qtype, dtype, &s);
     if (st) return st;
     if (M < 0 || M > kMaxDim) return fail(W4A16_ERR_INVALID_ARG, "M=%lld out of range", (long long)M);
+    const int opts = path & ~0xFF;
+    path &= 0xFF;
+    if (opts & ~W4A16_OPT_STATIC_WEIGHTS) return fail(W4A16_ERR_INVALID_ARG, "unknown option bits 0x%x", opts);
     if (path < W4A16_PATH_AUTO || path > W4A16_PATH_DENSE) return fail(W4A16_ERR_INVALID_ARG, "unknown path %d", path);
     st = check_qptrs(Wq, scales, zeros, qtype);
     if (st) return st;
@@ -285,7 +313,8 @@ w4a16_status w4a16_gemm_ex(const void* A, const void* Wq, const void* scales,
     g_err[0] = '\0';
     if (M == 0) return W4A16_OK;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    if (path == W4A16_PATH_DECODE) return launch_decode_path(A, Wq, scales, zeros, C, s, cs);
+    if (path == W4A16_PATH_DECODE)
+        return launch_decode_path(A, Wq, scales, zeros, C, s, (opts & W4A16_OPT_STATIC_WEIGHTS) != 0, cs);
     if (path == W4A16_PATH_DENSE) return launch_tcgen05(A, Wdense, true, nullptr, nullptr, C, s, cs);
     return launch_tcgen05(A, Wq, false, scales, zeros, C, s, cs);
 }
@@ -331,6 +360,8 @@ w4a16_status w4a16_gemm_dense(const void* A, const void* W, void* C, int64_t M, 
     s.g_eff = K;
     s.ng = 1;
     s.ldq = (K / 8 + 3) / 4 * 4;
+    s.lds = (N + 7) / 8 * 8;
+    s.ldz = (N / 8 + 3) / 4 * 4;
     s.bf16 = dtype == W4A16_BF16;
     s.zp = false;
     return launch_tcgen05(A, W, true, nullptr, nullptr, C, s, static_cast<cudaStream_t>(stream));
