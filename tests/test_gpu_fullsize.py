@@ -1,0 +1,129 @@
+"""Parity at the full workload sizes, in the launch configuration the benchmark
+uses (w4a16_gemm_ex through the C ABI on the current stream).
+
+Where the oracle finishes in seconds the whole output is compared; for the
+prefill and 70B-MLP shapes the oracle computes a deterministic sample: every
+output column for 8-16 sampled rows plus 4096 random (m, n) pairs, and the
+tolerance denominator max|C_ref| is taken over that sample.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+from w4a16_int4_weight_gb300 import inputs as synth
+
+from gpu_helpers import TOL, DeviceWeight, assert_device_status_ok, run_gemm
+
+pytestmark = pytest.mark.gpu
+
+
+def _check(C_bits, C_ref, dtype, what):
+    Cv = orc.values(C_bits, dtype)
+    assert np.all(np.isfinite(Cv)), what
+    err = orc.rel_error(Cv, C_ref)
+    assert err <= TOL[dtype], (what, err)
+    return err
+
+
+def _sampled_ref(A, W_ref, dtype, rows, pairs):
+    ref_rows = orc.gemm_rows(A, W_ref, rows, dtype)
+    ref_pairs = orc.gemm_pairs(A, W_ref, pairs[0], pairs[1], dtype)
+    return ref_rows, ref_pairs
+
+
+def _check_sampled(C, ref_rows, ref_pairs, rows, pairs, dtype, what):
+    got_rows = C[rows]
+    got_pairs = C[pairs[0], pairs[1]]
+    ref = np.concatenate([ref_rows.ravel(), ref_pairs])
+    got = np.concatenate([got_rows.ravel(), got_pairs])
+    return _check(got, ref, dtype, what)
+
+
+def _sample(M, N, nrows, npairs, seed):
+    rng = np.random.default_rng(seed)
+    rows = np.unique(np.concatenate([[0, M - 1], rng.integers(0, M, max(0, nrows - 2))]))
+    pairs = (rng.integers(0, M, npairs), rng.integers(0, N, npairs))
+    return rows, pairs
+
+
+@pytest.mark.parametrize("p", synth.WORKLOADS["decode_k4096_n4096_g128_u4b8_bf16"],
+                         ids=lambda p: f"M{p.M}")
+def test_decode_gemv_7b_attention_shape_full(p):
+    x = synth.make_inputs(p)
+    C_ref = orc.linear(x.A, x.q, x.scales, x.zeros, p.group_size, p.dtype)
+    w = DeviceWeight(p, x.q, x.scales, x.zeros)
+    C = run_gemm(w, x.A, path="auto")
+    _check(C, C_ref, p.dtype, "auto")
+    assert_device_status_ok()
+
+
+@pytest.mark.parametrize("p", synth.WORKLOADS["zp_m16_g32_bf16_mlp_pair"],
+                         ids=lambda p: f"K{p.K}_N{p.N}")
+def test_zero_point_mlp_pair_full(p):
+    x = synth.make_inputs(p)
+    C_ref = orc.linear(x.A, x.q, x.scales, x.zeros, p.group_size, p.dtype)
+    w = DeviceWeight(p, x.q, x.scales, x.zeros)
+    for path in ("auto", "decode", "fused"):
+        _check(run_gemm(w, x.A, path=path), C_ref, p.dtype, path)
+    assert_device_status_ok()
+
+
+def test_gemv_k512_full():
+    p = synth.WORKLOADS["gemv_m1_k512_n512_g128_u4b8_fp16"][0]
+    x = synth.make_inputs(p)
+    C_ref = orc.linear(x.A, x.q, x.scales, x.zeros, p.group_size, p.dtype)
+    w = DeviceWeight(p, x.q, x.scales, x.zeros)
+    for path in ("auto", "decode", "fused"):
+        _check(run_gemm(w, x.A, path=path), C_ref, p.dtype, path)
+
+
+def test_prefill_8b_mlp_up_sampled():
+    p = synth.WORKLOADS["prefill_m2048_k4096_n14336_g128_u4b8_bf16"][0]
+    x = synth.make_inputs(p)
+    W_ref = orc.dequant(x.q, x.scales, x.zeros, p.group_size, p.dtype)
+    rows, pairs = _sample(p.M, p.N, 16, 4096, 1)
+    ref_rows, ref_pairs = _sampled_ref(x.A, W_ref, p.dtype, rows, pairs)
+    w = DeviceWeight(p, x.q, x.scales, x.zeros)
+    Wd = w.dequant()
+    from gpu_helpers import to_host_bits
+    # the dense copy itself is bit-exact at full size
+    assert np.array_equal(to_host_bits(Wd), W_ref)
+    for path in ("auto", "fused", "dense"):
+        C = run_gemm(w, x.A, path=path, Wdense=Wd if path == "dense" else None)
+        _check_sampled(C, ref_rows, ref_pairs, rows, pairs, p.dtype, path)
+    assert_device_status_ok()
+
+
+# The 70B-MLP crossover shape: every (group size, quant type, dtype) combination,
+# each at two of the sweep's M values so that all twelve M values are covered.
+_SWEEP_M = (1, 2, 4, 8, 16, 32, 64, 128, 256, 512, 1024, 4096)
+_COMBOS = [(g, qt, dt) for g in (-1, 64, 256) for qt in ("uint4b8", "uint4") for dt in ("fp16", "bf16")]
+
+
+@pytest.fixture(scope="module")
+def sweep_q():
+    p = synth.Problem(1, 28672, 8192, 64, "uint4b8", "bf16")
+    return synth.make_weights(p)[0]
+
+
+@pytest.mark.parametrize("ci", range(len(_COMBOS)),
+                         ids=lambda i: "G{}_{}_{}".format(*_COMBOS[i]))
+def test_crossover_70b_mlp_sampled(sweep_q, ci):
+    G, qt, dt = _COMBOS[ci]
+    Ms = (_SWEEP_M[ci % 12], _SWEEP_M[(ci + 6) % 12])
+    Mmax = max(Ms)
+    p = synth.Problem(Mmax, 28672, 8192, G, qt, dt)
+    s, z = synth.make_scales(p), synth.make_zeros(p)
+    A = synth.make_activations(p)
+    W_ref = orc.dequant(sweep_q, s, z, G, dt)
+    w = DeviceWeight(p, sweep_q, s, z)
+    for M in Ms:
+        rows, pairs = _sample(M, p.N, 8, 4096, ci * 100 + M)
+        ref_rows, ref_pairs = _sampled_ref(A[:M], W_ref, dt, rows, pairs)
+        C = run_gemm(w, A[:M], path="auto")
+        _check_sampled(C, ref_rows, ref_pairs, rows, pairs, dt, f"M={M}")
+    del w
+    torch.cuda.empty_cache()
+    assert_device_status_ok()

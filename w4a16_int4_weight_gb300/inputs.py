@@ -152,17 +152,23 @@ class Inputs:
     A: np.ndarray            # uint16 bits [M, K] of dtype
 
 
-def make_weights(p: Problem):
-    q = nibbles(p.seed, STREAM_Q, p.N * p.K).reshape(p.N, p.K)
+def make_scales(p: Problem) -> np.ndarray:
     ng = p.ngroups
     s64 = p.scale_lo + (p.scale_hi - p.scale_lo) * uniform01(p.seed, STREAM_SCALES, p.N * ng)
-    scales = to_dtype_bits(s64, p.dtype).reshape(p.N, ng)
-    zeros = None
-    if p.qtype == "uint4":
-        if p.N % 8:
-            raise ValueError("explicit zero points need N % 8 == 0")
-        zeros = words32(p.seed, STREAM_ZEROS, (p.N // 8) * ng).reshape(p.N // 8, ng)
-    return q, scales, zeros
+    return to_dtype_bits(s64, p.dtype).reshape(p.N, ng)
+
+
+def make_zeros(p: Problem):
+    if p.qtype != "uint4":
+        return None
+    if p.N % 8:
+        raise ValueError("explicit zero points need N % 8 == 0")
+    return words32(p.seed, STREAM_ZEROS, (p.N // 8) * p.ngroups).reshape(p.N // 8, p.ngroups)
+
+
+def make_weights(p: Problem):
+    q = nibbles(p.seed, STREAM_Q, p.N * p.K).reshape(p.N, p.K)
+    return q, make_scales(p), make_zeros(p)
 
 
 def make_activations(p: Problem) -> np.ndarray:
