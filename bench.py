@@ -513,7 +513,7 @@ def main():
     t_launch = t_dev / (args.steps * launches_per_step)
     achieved = (abytes_step / launches_per_step) / t_launch / 1e9
     traffic = profiled_traffic("decode_kernel_m1_4_8_k4096_n4096.md",
-                               ["decode.cu", "common.cuh"], 1)
+                               ["decode_kernel.cuh", "decode.cu", "common.cuh"], 1)
 
     cpu = None
     if rank == 0:
