@@ -39,7 +39,7 @@ bool plan_decode(int64_t M, int64_t N, int64_t K, int num_sms, int* ks_out, int*
                  size_t* smem_out, int* nt_out);
 
 // prefill.cu: tcgen05 GEMM, fused-dequant (Wq != null) or dense (tmap_w dense).
-// maps: A [M][K] box {64,BT} SW128; weights (packed [N][ldq] box {8,128}, or
+// maps: A [M][K] box {64,BT} SW128; weights (packed [N][ldq] box {8,128} SW32, or
 // dense [N][K] box {64,128} SW128); scales [ng][lds] box {128,2}; zeros [ng][ldz] box {16,2}.
 cudaError_t launch_prefill(const CUtensorMap* maps, void* C, const LayerShape& s, bool dense,
                            int token_tile, cudaStream_t stream);

@@ -5,16 +5,17 @@
 // scale and feeds a dot product with fp32 accumulation.  Here the same tile
 // algebra runs as a warp-specialised tcgen05 pipeline:
 //
-//   warp 4     TMA producer: per 64-wide K block, the activation tile
+//   warp 8     TMA producer: per 64-wide K block, the activation tile
 //              [BT tokens x 64] (128-byte swizzle) and either the packed weight
-//              tile [128 rows x 8 words] (fused) or the dense weight tile
-//              [128 x 64] (dense path), into a 4-stage ring.
-//   warps 0-3  dequantisers (fused path): thread i owns weight row i of the
-//              tile, unpacks 64 K-values with LOP3 magic-number unpacks, forms
-//              rne((q - z) * s) exactly as the pages do, and stores the bf16/fp16
-//              tile in the 128-byte-swizzled K-major layout the tensor core
-//              reads.  After the K loop the same warps are the epilogue.
-//   warp 5     allocates TMEM and issues tcgen05.mma (one thread): the weight
+//              tile [128 rows x 8 words] (32-byte swizzle) with its scale and
+//              zero-point rows (fused), or the dense weight tile [128 x 64]
+//              (dense path), into a 4-stage ring.
+//   warps 0-7  dequantisers (fused path): thread i owns half of weight row
+//              i % 128 (32 K-values), unpacks with LOP3 magic-number unpacks,
+//              forms rne((q - z) * s) exactly as the pages do, and stores the
+//              bf16/fp16 tile in the 128-byte-swizzled K-major layout the tensor
+//              core reads.  After the K loop the same warps are the epilogue.
+//   warp 9     allocates TMEM and issues tcgen05.mma (one thread): the weight
 //              tile is the MMA's A operand (M = 128 weight rows), the activation
 //              tile the B operand (N = BT tokens), fp32 accumulator in TMEM, so
 //              each dequantised weight feeds BT multiply-adds.
@@ -30,13 +31,17 @@ namespace {
 constexpr int kBM = 128;                  // weight rows per CTA (UMMA M)
 constexpr int kBK = 64;                   // K per stage: one 128-byte swizzle row of 16-bit values
 constexpr int kStages = 4;
-constexpr int kThreads = 192;
+constexpr int kDqWarps = 8;               // dequantiser / epilogue warps
+constexpr int kProducerWarp = kDqWarps;
+constexpr int kMmaWarp = kDqWarps + 1;
+constexpr int kThreads = (kDqWarps + 2) * 32;
 constexpr int kWtBytes = kBM * 128;       // 16 KB dequantised / dense weight tile
 constexpr int kPkBytes = kBM * 32;        // 4 KB packed tile (8 words per row)
 constexpr int kScBytes = 2 * kBM * 2;     // scales of two groups x 128 rows
 constexpr int kZpBytes = 2 * 16 * 4;      // zero-point words of two groups x 128 rows
 
 __device__ int g_status;
+__device__ __forceinline__ int* p_status() { return &g_status; }
 
 struct Params {
     uint16_t* C;
@@ -85,13 +90,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&dq_full[s], 4);
+            mbar_init(&dq_full[s], kDqWarps);
             mbar_init(&empty[s], 1);
         }
         mbar_init(acc_full, 1);
         fence_mbar_init();
     }
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         tmem_alloc(tmem_slot, BT);
         tmem_relinquish();
     }
@@ -100,7 +105,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     tc_fence_after();
     const uint32_t tmem_d = *tmem_slot;
 
-    if (warp == 4) {
+    if (warp == kProducerWarp) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
             tma_prefetch_desc(&tmap_a);
@@ -111,7 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             for (int kb = 0; kb < p.nkb && ok; ++kb) {
                 const int s = kb % kStages;
                 if (kb >= kStages)
-                    ok = mbar_wait(&empty[s], uint32_t(kb / kStages - 1) & 1u, &g_status, 10);
+                    ok = mbar_wait(&empty[s], uint32_t(kb / kStages - 1) & 1u, p_status(), 10);
                 if (!ok) break;
                 mbar_arrive_expect_tx(&full[s], L::kActBytes + (DENSE ? kWtBytes
                                                      : kPkBytes + kScBytes + (ZP ? kZpBytes : 0)));
@@ -129,9 +134,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             }
             // copies still in flight must land before the CTA can retire
             for (int kb = max(0, issued - kStages); kb < issued; ++kb)
-                mbar_wait(&full[kb % kStages], uint32_t(kb / kStages) & 1u, &g_status, 11);
+                mbar_wait(&full[kb % kStages], uint32_t(kb / kStages) & 1u, p_status(), 11);
         }
-    } else if (warp == 5) {
+    } else if (warp == kMmaWarp) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f16(BF16, kBM, BT);
@@ -139,8 +144,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             for (int kb = 0; kb < p.nkb && ok; ++kb) {
                 const int s = kb % kStages;
                 const uint32_t par = uint32_t(kb / kStages) & 1u;
-                ok = mbar_wait(&full[s], par, &g_status, 12);
-                if (ok && !DENSE) ok = mbar_wait(&dq_full[s], par, &g_status, 13);
+                ok = mbar_wait(&full[s], par, p_status(), 12);
+                if (ok && !DENSE) ok = mbar_wait(&dq_full[s], par, p_status(), 13);
                 if (!ok) break;
                 tc_fence_after();
                 const uint64_t a_desc = smem_desc_sw128(wt_tile(s));
@@ -153,48 +158,42 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             if (ok) umma_commit(acc_full);
         }
     } else {
-        // ---------------- dequantisers (warps 0-3), then epilogue ----------------
-        const int row = tid;                 // weight row within the tile
-        const int n = n0 + row;
-        const bool row_ok = n < p.N;        // rows past N read zero-filled tiles
+        // ---------------- dequantisers (warps 0-7), then epilogue ----------------
+        const int row = tid & (kBM - 1);     // weight row within the tile
+        const int half = tid >> 7;           // K-values 32*half .. +31 of each block
         bool ok = true;
         if constexpr (!DENSE) {
             for (int kb = 0; kb < p.nkb; ++kb) {
                 const int s = kb % kStages;
                 // warp-uniform outcome: the warp leaves the loop together or not at all
-                ok = __all_sync(0xffffffffu, mbar_wait(&full[s], uint32_t(kb / kStages) & 1u, &g_status, 14));
+                ok = __all_sync(0xffffffffu, mbar_wait(&full[s], uint32_t(kb / kStages) & 1u, p_status(), 14));
                 if (!ok) break;
-                const uint4* src = reinterpret_cast<const uint4*>(pk_tile(s) + row * 32);
-                const uint4 wa = src[0], wb = src[1];
-                const uint32_t words[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
-                // words 0-3 (K-values kb*64 + 0..31) and 4-7 (+32..63) each lie in one
-                // group: every group size is a multiple of 32, or there is one group.
-                // The second half uses the tile's second group row only when G = 32.
-                const int gb = (p.g_eff == 32 && p.ng > 1) ? 1 : 0;
-                const uint16_t* sc = sc_tile(s);
-                const uint32_t sa = sc[row], sb = sc[gb * kBM + row];
-                const uint32_t s2a = sa | (sa << 16), s2b = sb | (sb << 16);
-                int za = 8, zb = 8;
-                if constexpr (ZP) {
-                    const uint32_t* zt = zp_tile(s);
-                    za = (zt[row >> 3] >> (4 * (row & 7))) & 0xF;
-                    zb = (zt[gb * 16 + (row >> 3)] >> (4 * (row & 7))) & 0xF;
-                }
-                const ZeroConst zca = make_zero_const<BF16>(za);
-                const ZeroConst zcb = make_zero_const<BF16>(zb);
+                // 32-byte-swizzled packed row: 16-byte chunk h sits at chunk h ^ ((row / 4) % 2)
+                const uint4 wq = *reinterpret_cast<const uint4*>(
+                    pk_tile(s) + row * 32 + ((half ^ ((row >> 2) & 1)) << 4));
+                const uint32_t words[4] = {wq.x, wq.y, wq.z, wq.w};
+                // the 32 K-values lie in one group: every group size is a multiple of
+                // 32, or there is one group; the tile's second group row is the
+                // K block's second half when G = 32
+                const int gl = (p.g_eff == 32 && p.ng > 1) ? half : 0;
+                const uint32_t sv = sc_tile(s)[gl * kBM + row];
+                const uint32_t s2 = sv | (sv << 16);
+                int z = 8;
+                if constexpr (ZP) z = (zp_tile(s)[gl * 16 + (row >> 3)] >> (4 * (row & 7))) & 0xF;
+                const ZeroConst zc = make_zero_const<BF16>(z);
                 uint8_t* dst = wt_tile(s) + row * 128;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
+                for (int j = 0; j < 4; ++j) {
                     uint32_t q[4];
-                    unpack_word<BF16>(words[j], j < 4 ? zca : zcb, q);
-                    const uint32_t s2 = j < 4 ? s2a : s2b;
+                    unpack_word<BF16>(words[j], zc, q);
                     uint4 o;
                     o.x = scale_pair<BF16>(q[0], s2);
                     o.y = scale_pair<BF16>(q[1], s2);
                     o.z = scale_pair<BF16>(q[2], s2);
                     o.w = scale_pair<BF16>(q[3], s2);
-                    // 16-byte chunk j of this 128-byte row goes to chunk j ^ (row % 8)
-                    *reinterpret_cast<uint4*>(dst + ((j ^ (row & 7)) << 4)) = o;
+                    // 16-byte chunk c of this 128-byte row goes to chunk c ^ (row % 8)
+                    const int c = 4 * half + j;
+                    *reinterpret_cast<uint4*>(dst + ((c ^ (row & 7)) << 4)) = o;
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -202,13 +201,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             }
         }
         // ---------------- epilogue ----------------
-        if (ok) ok = mbar_wait(acc_full, 0u, &g_status, 15);
+        if (ok) ok = mbar_wait(acc_full, 0u, p_status(), 15);
         ok = __all_sync(0xffffffffu, ok);   // tcgen05.ld below is warp-collective
         tc_fence_after();
         if (ok) {
-            const uint32_t lane_base = uint32_t(32 * warp) << 16;
+            // warp w reads TMEM lanes 32*(w%4).. (its rows) and half w/4 of the columns
+            const uint32_t lane_base = uint32_t(32 * (warp & 3)) << 16;
+            const int n_out = n0 + 32 * (warp & 3) + lane;
+            const bool row_ok = n_out < p.N;
 #pragma unroll 1
-            for (int c = 0; c < BT / 32; ++c) {
+            for (int c = (warp >> 2) * (BT / 64); c < ((warp >> 2) + 1) * (BT / 64); ++c) {
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(tmem_d + lane_base + uint32_t(32 * c), r);
                 tmem_ld_wait();
@@ -217,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const int tok = tok0 + j;
-                        if (tok < p.M) p.C[size_t(tok) * p.N + n] = from_f32<BF16>(__uint_as_float(r[j]));
+                        if (tok < p.M) p.C[size_t(tok) * p.N + n_out] = from_f32<BF16>(__uint_as_float(r[j]));
                     }
                 }
             }
@@ -225,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) tmem_dealloc(tmem_d, BT);
+    if (warp == kMmaWarp) tmem_dealloc(tmem_d, BT);
 }
 
 template <bool BF16, bool ZP, int BT, bool DENSE>

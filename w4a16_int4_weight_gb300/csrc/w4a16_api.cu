@@ -180,7 +180,7 @@ w4a16_status launch_tcgen05(const void* A, const void* Wsrc, bool dense, const v
         maps[3] = maps[0];
     } else {
         st = make_map(&maps[1], Wsrc, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, uint64_t(s.ldq), uint64_t(s.N),
-                      uint64_t(s.ldq) * 4, 8, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
+                      uint64_t(s.ldq) * 4, 8, 128, CU_TENSOR_MAP_SWIZZLE_32B);
         if (st) return st;
         st = make_map(&maps[2], scales, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, uint64_t(s.lds),
                       uint64_t(s.ng), uint64_t(s.lds) * 2, 128, 2, CU_TENSOR_MAP_SWIZZLE_NONE);
