@@ -65,7 +65,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true", help="skip the prefill/zero-point side measurements")
-    ap.add_argument("--profile-case", choices=["decode", "zp", "prefill", "dense", "dequant"],
+    ap.add_argument("--profile-case", choices=["decode", "decode_large", "zp", "prefill", "dense", "dequant"],
                     help="only run `--reps` eager launches of one kernel (for ncu), then exit")
     ap.add_argument("--reps", type=int, default=8)
     return ap.parse_args()
@@ -369,8 +369,10 @@ def profile_case(args):
     from w4a16_int4_weight_gb300 import inputs as synth
     tdt = torch.bfloat16
     c = args.profile_case
-    if c in ("decode", "zp"):
-        M, N, K, G, qt = (8, N_, K_, G_, QTYPE) if c == "decode" else (16, 11008, 4096, 32, "uint4")
+    if c in ("decode", "decode_large", "zp"):
+        M, N, K, G, qt = {"decode": (8, N_, K_, G_, QTYPE),
+                          "decode_large": (1, 28672, 8192, 64, QTYPE),
+                          "zp": (16, 11008, 4096, 32, "uint4")}[c]
         lay = make_layers(torch, B, synth, 4, M, N, K, G, qt, "bf16")
         A = torch.randn(M, K, device="cuda").to(tdt)
         C = torch.empty(M, N, dtype=tdt, device="cuda")

@@ -11,10 +11,13 @@ namespace {
 
 __device__ int g_status;
 
-int stage_bytes_for(int64_t M) {
+// Activation sub-box slot: 8 * NT token rows of 64 bytes (the kernel's compile-time size).
+int a_slot_for(int64_t M) { return 512 * (M <= 8 ? 1 : M <= 16 ? 2 : M <= 32 ? 4 : 8); }
+
+int stage_bytes_for(int64_t M, int gps, bool zp) {
     using namespace decode;
-    const int a_slot = int((M + 7) / 8 * 8) * 64;
-    const int raw = kWBytes + (kBoxK / kSubK) * a_slot + kMaxGps * kBN * 2 + kMaxGps * 16 * 4;
+    const int a_slot = a_slot_for(M);
+    const int raw = kWBytes + (kBoxK / kSubK) * a_slot + gps * kBN * 2 + (zp ? gps * 16 * 4 : 0);
     return (raw + 1023) / 1024 * 1024;
 }
 
@@ -43,10 +46,10 @@ int decode_scale_box_rows(int64_t g_eff, int64_t ng) {
 }
 
 // Host-side plan for a shape: cluster size (K split), ring depth, shared memory.
-// K is split over up to 8 CTAs until there are about three CTAs per SM; each
+// K is split over up to 8 CTAs until there are about three CTAs per SM.  Each
 // ring stage holds one 256-wide K box.
-bool plan_decode(int64_t M, int64_t N, int64_t K, int num_sms, int* ks_out, int* stages_out,
-                 size_t* smem_out, int* nt_out) {
+bool plan_decode(int64_t M, int64_t N, int64_t K, int64_t g_eff, int64_t ng, bool zp,
+                 int num_sms, int* ks_out, int* stages_out, size_t* smem_out, int* nt_out) {
     using namespace decode;
     if (M < 1 || M > kDecodeMaxM) return false;
     const int nt = M <= 8 ? 1 : M <= 16 ? 2 : M <= 32 ? 4 : 8;
@@ -56,15 +59,35 @@ bool plan_decode(int64_t M, int64_t N, int64_t K, int num_sms, int* ks_out, int*
     int ks = 1;
     while (ks < 8 && row_tiles * ks < target && 2 * ks <= nboxes) ks *= 2;
     const int64_t boxes_per = (nboxes + ks - 1) / ks;
-    const int sb = stage_bytes_for(M);
+    const int sb = stage_bytes_for(M, decode_scale_box_rows(g_eff, ng), zp);
     const size_t red = ks > 1 ? size_t(kBN) * 8 * nt * 4 : 0;
-    // two stages keep a box in flight behind the one being consumed; more
-    // stages only while they still leave room for three CTAs per SM
-    int want = int(boxes_per < 2 ? boxes_per : 2);
-    for (int s = 3; s <= kMaxStages && s <= boxes_per; ++s)
-        if (size_t(s) * sb + red + 2048 <= 74 * 1024) want = s;
-    for (int stages = want; stages >= 1; --stages) {
-        const size_t smem = size_t(stages) * sb + 128 + red + 1024;
+    auto smem_for = [&](int s) { return size_t(s) * sb + 128 + red + 1024; };
+    const size_t sm_bytes = 228 * 1024;
+    const int max_ctas = nt == 1 ? 4 : nt == 2 ? 3 : 1;   // register limit of the instantiations
+    // Pick the depth: at least ~96 KB of weight boxes in flight per SM (enough to
+    // cover HBM latency at full bandwidth), then as many resident CTAs (consumer
+    // warps) as possible, then the shallowest ring.
+    int best = 1;
+    long best_ctas = -1, best_inflight = -1;
+    bool best_ok = false;
+    for (int s = 1; s <= kMaxStages && s <= boxes_per; ++s) {
+        const size_t sm = smem_for(s);
+        if (sm > 227 * 1024) break;
+        long ctas = long(sm_bytes / (sm + 1024));
+        if (ctas > max_ctas) ctas = max_ctas;
+        const long ahead = s == boxes_per ? s : s - 1;
+        const long inflight = ctas * ahead * kWBytes;
+        const bool ok = inflight >= 96 * 1024;
+        const bool better = ok ? (!best_ok || ctas > best_ctas) : (!best_ok && inflight > best_inflight);
+        if (better) {
+            best = s;
+            best_ctas = ctas;
+            best_inflight = inflight;
+            best_ok = ok;
+        }
+    }
+    for (int stages = best; stages >= 1; --stages) {
+        const size_t smem = smem_for(stages);
         if (smem <= 227 * 1024) {
             *ks_out = ks;
             *stages_out = stages;
@@ -81,7 +104,8 @@ cudaError_t launch_decode(const CUtensorMap* maps, void* C, const LayerShape& s,
     using namespace decode;
     int ks, stages, nt;
     size_t smem;
-    if (!plan_decode(s.M, s.N, s.K, num_sms, &ks, &stages, &smem, &nt)) return cudaErrorInvalidValue;
+    if (!plan_decode(s.M, s.N, s.K, s.g_eff, s.ng, s.zp, num_sms, &ks, &stages, &smem, &nt))
+        return cudaErrorInvalidValue;
     Params p;
     p.C = static_cast<uint16_t*>(C);
     p.status = status_ptr();
@@ -95,8 +119,8 @@ cudaError_t launch_decode(const CUtensorMap* maps, void* C, const LayerShape& s,
     p.stages = stages;
     p.gps = decode_scale_box_rows(s.g_eff, s.ng);
     if (p.gps < 1 || p.gps > kMaxGps) return cudaErrorInvalidValue;   // never expected
-    p.a_slot = int((s.M + 7) / 8 * 8) * 64;
-    p.stage_bytes = stage_bytes_for(s.M);
+    p.a_slot = a_slot_for(s.M);
+    p.stage_bytes = stage_bytes_for(s.M, p.gps, s.zp);
     p.red_off = stages * p.stage_bytes + 128;
     p.prefetch_weights = prefetch_weights ? 1 : 0;
     const int wpg = (s.ng == 1 || s.g_eff >= kBoxK) ? 8 : int(s.g_eff / 32);

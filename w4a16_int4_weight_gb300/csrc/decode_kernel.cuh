@@ -32,6 +32,8 @@
 
 #include <cooperative_groups.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -46,7 +48,7 @@ constexpr int kBN = 16 * kConsumerWarps;               // weight rows per CTA
 constexpr int kBoxK = 256;               // K-values per box (32 words = 128 bytes per row)
 constexpr int kWBytes = kBN * 128;       // 16 KB packed weight box
 constexpr int kSubK = 32;                // K-values per activation sub-box (64 bytes per row)
-constexpr int kMaxStages = 4;
+constexpr int kMaxStages = 8;
 constexpr int kMaxGps = 8;               // groups per box at G = 32
 
 struct Params {
@@ -57,8 +59,9 @@ struct Params {
     int ks;           // CTAs per cluster (K split)
     int stages;       // ring depth (<= kMaxStages)
     int gps;          // scale-tile rows per box
-    int a_slot;       // bytes of one [round_up(M,8) x 32] activation sub-box slot
-    int stage_bytes;  // bytes per stage (multiple of 1024)
+    int a_slot;       // bytes of one activation sub-box slot: [8 * NT rows][32 values] = 512 * NT
+    int stage_bytes;  // bytes per stage (multiple of 1024): weights, activations, gps scale
+                      // rows of 256 bytes and, with zero points, gps rows of 64 bytes
     int red_off;      // byte offset of the cluster reduction buffer
     int prefetch_weights;   // weights may be read before the previous grid completes
 };
@@ -74,8 +77,8 @@ __device__ __forceinline__ StageView stage_view(uint8_t* base, const Params& p, 
     StageView v;
     v.w = base + s * p.stage_bytes;
     v.a = v.w + kWBytes;
-    v.sc = reinterpret_cast<uint16_t*>(v.a + 8 * p.a_slot);
-    v.zp = reinterpret_cast<uint32_t*>(v.sc + kMaxGps * kBN);
+    v.sc = reinterpret_cast<uint16_t*>(v.a + 8 * p.a_slot);   // a_slot = 512 * NT
+    v.zp = reinterpret_cast<uint32_t*>(v.sc + p.gps * kBN);
     return v;
 }
 
@@ -105,7 +108,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
                                                           const __grid_constant__ CUtensorMap tmap_z,
                                                           const Params p) {
     constexpr int MP = 8 * NT;                      // padded token count of the MMA column tiles
-    constexpr int NSETS = NT >= 4 ? 1 : 4 / NT;     // independent accumulator chains per tile
+    constexpr int NSETS = NT == 1 ? 2 : 1;          // independent accumulator chains per tile
+    constexpr int kASlot = 512 * NT;                // == p.a_slot: [8 * NT rows][32 values] sub-box
     constexpr int GPB = 8 / WPG;                    // groups per box (1 in the large-group mode)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -195,6 +199,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
         ZeroConst zc0 = make_zero_const<BF16>(8), zc1 = zc0;
         int cur_g = -1;   // large-group mode: group whose sums accg holds
 
+        // acc += scale * group sum.  In the per-group modes the next group's first
+        // MMAs overwrite accg (zero accumulator input), so nothing is cleared here.
         auto flush = [&]() {
 #pragma unroll
             for (int j = 0; j < NT; ++j) {
@@ -204,8 +210,6 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
                     v[e] = accg[0][j][e];
 #pragma unroll
                     for (int c = 1; c < NSETS; ++c) v[e] += accg[c][j][e];
-#pragma unroll
-                    for (int c = 0; c < NSETS; ++c) accg[c][j][e] = 0.f;
                 }
                 acc[j][0] = fmaf(s0, v[0], acc[j][0]);
                 acc[j][1] = fmaf(s0, v[1], acc[j][1]);
@@ -222,13 +226,59 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
             }
         };
         // per-thread shared-memory offsets that do not depend on the stage
-        const int wrow0 = r0 * 128 + (t << 2), wrow1 = r1 * 128 + (t << 2);
+        const int wrow0 = r0 * 128 + (t << 2);     // row r1 = r0 + 8 is 1024 bytes further
+        const int g16 = g << 4;
         int aoff[NT];
+        bool tok_ok[NT];
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
             const int tok = 8 * j + g;
             aoff[j] = tok * 64 + ((t ^ ((tok >> 1) & 3)) << 4);
+            tok_ok[j] = tok < p.M;
         }
+
+        // One K box; CHECK: the box may end early at k_hi (the last box of a K range).
+        auto run_box = [&](const StageView& v, int box_k, auto check_tag) {
+            constexpr bool CHECK = decltype(check_tag)::value;
+#pragma unroll
+            for (int gi = 0; gi < GPB; ++gi) {
+                if (CHECK && box_k + gi * WPG * 32 >= k_hi) break;
+                if constexpr (WPG < 8) load_group(v, gi);
+#pragma unroll
+                for (int w = 0; w < WPG; ++w) {
+                    const int ws = gi * WPG + w;
+                    if (CHECK && box_k + ws * 32 >= k_hi) break;
+                    // word ws*4 + t of the box row: 16-byte chunk ws sits at chunk ws ^ (row % 8)
+                    const uint8_t* wp = v.w + wrow0 + ((ws << 4) ^ g16);
+                    const uint32_t w0 = *reinterpret_cast<const uint32_t*>(wp);
+                    const uint32_t w1 = *reinterpret_cast<const uint32_t*>(wp + 1024);
+                    uint32_t q0[4], q1[4];
+                    unpack_word<BF16>(w0, zc0, q0);
+                    unpack_word<BF16>(w1, zc1, q1);
+                    const uint32_t a_s0[4] = {q0[0], q1[0], q0[1], q1[1]};
+                    const uint32_t a_s1[4] = {q0[2], q1[2], q0[3], q1[3]};
+                    // activation K-values kw + 8t .. +7: sub-box ws, 16-byte chunk t, which
+                    // the 64-byte swizzle places at chunk t ^ ((row / 2) % 4)
+                    const uint8_t* abox = v.a + ws * kASlot;
+#pragma unroll
+                    for (int j = 0; j < NT; ++j) {
+                        uint4 b = make_uint4(0u, 0u, 0u, 0u);
+                        if (tok_ok[j]) b = *reinterpret_cast<const uint4*>(abox + aoff[j]);
+                        // step st = 2w + s of the group goes to set st % NSETS; a set's
+                        // first step in a group starts from zero (per-group modes)
+                        if (WPG < 8 && w == 0) {
+                            mma_m16n8k16<BF16, true>(accg[0][j], a_s0, b.x, b.y);
+                            if constexpr (NSETS == 2) mma_m16n8k16<BF16, true>(accg[1][j], a_s1, b.z, b.w);
+                            else mma_m16n8k16<BF16>(accg[0][j], a_s1, b.z, b.w);
+                        } else {
+                            mma_m16n8k16<BF16>(accg[0][j], a_s0, b.x, b.y);
+                            mma_m16n8k16<BF16>(accg[NSETS - 1][j], a_s1, b.z, b.w);
+                        }
+                    }
+                }
+                if constexpr (WPG < 8) flush();
+            }
+        };
 
         for (int i = 0; i < nb; ++i) {
             const int stage = i % p.stages;
@@ -241,41 +291,18 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
                 const int grp = box_k / p.g_eff;
                 if (grp != cur_g) {
                     if (cur_g >= 0) flush();
+#pragma unroll
+                    for (int c = 0; c < NSETS; ++c)
+#pragma unroll
+                        for (int j = 0; j < NT; ++j)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) accg[c][j][e] = 0.f;
                     cur_g = grp;
                     load_group(v, 0);
                 }
             }
-#pragma unroll
-            for (int gi = 0; gi < GPB; ++gi) {
-                const int kw0 = box_k + gi * WPG * 32;
-                if (kw0 >= k_hi) break;
-                if constexpr (WPG < 8) load_group(v, gi);
-#pragma unroll
-                for (int w = 0; w < WPG; ++w) {
-                    const int ws = gi * WPG + w;
-                    if (kw0 + w * 32 >= k_hi) break;
-                    // word ws*4 + t of the box row: 16-byte chunk ws sits at chunk ws ^ (row % 8)
-                    const int woff = (ws ^ g) << 4;
-                    const uint32_t w0 = *reinterpret_cast<const uint32_t*>(v.w + wrow0 + woff);
-                    const uint32_t w1 = *reinterpret_cast<const uint32_t*>(v.w + wrow1 + woff);
-                    uint32_t q0[4], q1[4];
-                    unpack_word<BF16>(w0, zc0, q0);
-                    unpack_word<BF16>(w1, zc1, q1);
-                    const uint32_t a_s0[4] = {q0[0], q1[0], q0[1], q1[1]};
-                    const uint32_t a_s1[4] = {q0[2], q1[2], q0[3], q1[3]};
-                    // activation K-values kw + 8t .. +7: sub-box ws, 16-byte chunk t, which
-                    // the 64-byte swizzle places at chunk t ^ ((row / 2) % 4)
-                    const uint8_t* abox = v.a + ws * p.a_slot;
-#pragma unroll
-                    for (int j = 0; j < NT; ++j) {
-                        uint4 b = make_uint4(0u, 0u, 0u, 0u);
-                        if (8 * j + g < p.M) b = *reinterpret_cast<const uint4*>(abox + aoff[j]);
-                        mma_m16n8k16<BF16>(accg[(2 * ws) % NSETS][j], a_s0, b.x, b.y);
-                        mma_m16n8k16<BF16>(accg[(2 * ws + 1) % NSETS][j], a_s1, b.z, b.w);
-                    }
-                }
-                if constexpr (WPG < 8) flush();
-            }
+            if (box_k + kBoxK <= k_hi) run_box(v, box_k, std::false_type{});
+            else run_box(v, box_k, std::true_type{});
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stage]);
         }

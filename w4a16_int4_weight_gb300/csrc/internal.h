@@ -35,8 +35,8 @@ constexpr int64_t kDecodeMaxM = 64;
 cudaError_t launch_decode(const CUtensorMap* maps, void* C, const LayerShape& s, int num_sms,
                           bool prefetch_weights, cudaStream_t stream);
 int decode_scale_box_rows(int64_t g_eff, int64_t ng);
-bool plan_decode(int64_t M, int64_t N, int64_t K, int num_sms, int* ks_out, int* stages_out,
-                 size_t* smem_out, int* nt_out);
+bool plan_decode(int64_t M, int64_t N, int64_t K, int64_t g_eff, int64_t ng, bool zp,
+                 int num_sms, int* ks_out, int* stages_out, size_t* smem_out, int* nt_out);
 
 // prefill.cu: tcgen05 GEMM, fused-dequant (Wq != null) or dense (tmap_w dense).
 // maps: A [M][K] box {64,BT} SW128; weights (packed [N][ldq] box {8,128} SW32, or

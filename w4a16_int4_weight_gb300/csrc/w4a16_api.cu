@@ -147,11 +147,13 @@ w4a16_status device_sms(int* sms) {
 constexpr int64_t kDecodeUpToM = 32;
 constexpr int64_t kDenseFromM = 1024;
 
-int route_impl(int64_t M, int64_t N, int64_t K, bool has_dense) {
+int route_impl(const LayerShape& s, bool has_dense) {
+    const int64_t M = s.M;
     if (M <= kDecodeUpToM) {
         int ks, stages, nt;
         size_t smem;
-        if (plan_decode(M, N, K, 152, &ks, &stages, &smem, &nt)) return W4A16_PATH_DECODE;
+        if (plan_decode(M, s.N, s.K, s.g_eff, s.ng, s.zp, 152, &ks, &stages, &smem, &nt))
+            return W4A16_PATH_DECODE;
     }
     if (has_dense && M >= kDenseFromM) return W4A16_PATH_DENSE;
     return W4A16_PATH_FUSED;
@@ -278,9 +280,11 @@ w4a16_status w4a16_pack(const uint8_t* q, const void* scales, const int32_t* zer
 }
 
 int w4a16_route(int64_t M, int64_t N, int64_t K, int G, int qtype, int dtype, int has_dense) {
-    if (check_weight(N, K, G, qtype, dtype, nullptr) != W4A16_OK) return -1;
+    LayerShape s;
+    if (check_weight(N, K, G, qtype, dtype, &s) != W4A16_OK) return -1;
     if (M < 0 || M > kMaxDim) return -1;
-    return route_impl(M, N, K, has_dense != 0);
+    s.M = M;
+    return route_impl(s, has_dense != 0);
 }
 
 w4a16_status w4a16_gemm_ex(const void* A, const void* Wq, const void* scales,
@@ -301,13 +305,13 @@ w4a16_status w4a16_gemm_ex(const void* A, const void* Wq, const void* scales,
     if (!C || !aligned(C, 2)) return fail(W4A16_ERR_INVALID_ARG, "C must be a non-null 2-byte aligned device pointer");
     if (Wdense && !aligned(Wdense, 16)) return fail(W4A16_ERR_INVALID_ARG, "Wdense must be 16-byte aligned");
     s.M = M;
-    if (path == W4A16_PATH_AUTO) path = route_impl(M, N, K, Wdense != nullptr);
+    if (path == W4A16_PATH_AUTO) path = route_impl(s, Wdense != nullptr);
     if (path == W4A16_PATH_DENSE && !Wdense) return fail(W4A16_ERR_INVALID_ARG, "the dense path needs a dense copy (Wdense)");
     if (path == W4A16_PATH_DECODE) {
         int ks, stages, nt;
         size_t smem;
         if (M > kDecodeMaxM) return fail(W4A16_ERR_INVALID_ARG, "the decode path takes M <= %lld", (long long)kDecodeMaxM);
-        if (M > 0 && !plan_decode(M, N, K, 152, &ks, &stages, &smem, &nt))
+        if (M > 0 && !plan_decode(M, N, K, s.g_eff, s.ng, s.zp, 152, &ks, &stages, &smem, &nt))
             return fail(W4A16_ERR_UNSUPPORTED, "decode path: the activation slice for M=%lld, K=%lld does not fit in shared memory", (long long)M, (long long)K);
     }
     g_err[0] = '\0';
