@@ -11,13 +11,13 @@ namespace {
 
 __device__ int g_status;
 
-// Activation sub-box slot: 8 * NT token rows of 64 bytes (the kernel's compile-time size).
-int a_slot_for(int64_t M) { return 512 * (M <= 8 ? 1 : M <= 16 ? 2 : M <= 32 ? 4 : 8); }
+// Activation box slot: 8 * NT token rows of 256 values.
+int a_slot_for(int64_t M) { return 4096 * (M <= 8 ? 1 : M <= 16 ? 2 : M <= 32 ? 4 : 8); }
 
 int stage_bytes_for(int64_t M, int gps, bool zp) {
     using namespace decode;
     const int a_slot = a_slot_for(M);
-    const int raw = kWBytes + (kBoxK / kSubK) * a_slot + gps * kBN * 2 + (zp ? gps * 16 * 4 : 0);
+    const int raw = kWBytes + a_slot + gps * kBN * 2 + (zp ? gps * 16 * 4 : 0);
     return (raw + 1023) / 1024 * 1024;
 }
 

@@ -11,9 +11,9 @@
 //    workspace and no atomics are used.
 //  * Data movement.  A producer warp streams, per K box and on one mbarrier,
 //    the packed weight box [128 rows x 32 words] (128-byte swizzle), the
-//    activation box [M x 256] as eight [M x 32] sub-boxes (64-byte swizzle,
-//    zero-filled past K) and the box's scales and zero points from the
-//    transposed scale / zero sections.  Consumer warps release a stage through
+//    activation box [M x 256] (zero-filled past K) and the box's scales and zero
+//    points from the transposed scale / zero sections: three or four TMA
+//    operations per 16 KB of weights.  Consumer warps release a stage through
 //    a second mbarrier, so no CTA-wide barrier sits in the K loop.
 //  * Math.  Each consumer warp owns 16 rows.  A packed word (8 consecutive
 //    K-values of a row) is unpacked with one LOP3 per value pair into 16-bit
@@ -47,7 +47,6 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;   // + one producer warp
 constexpr int kBN = 16 * kConsumerWarps;               // weight rows per CTA
 constexpr int kBoxK = 256;               // K-values per box (32 words = 128 bytes per row)
 constexpr int kWBytes = kBN * 128;       // 16 KB packed weight box
-constexpr int kSubK = 32;                // K-values per activation sub-box (64 bytes per row)
 constexpr int kMaxStages = 8;
 constexpr int kMaxGps = 8;               // groups per box at G = 32
 
@@ -59,7 +58,7 @@ struct Params {
     int ks;           // CTAs per cluster (K split)
     int stages;       // ring depth (<= kMaxStages)
     int gps;          // scale-tile rows per box
-    int a_slot;       // bytes of one activation sub-box slot: [8 * NT rows][32 values] = 512 * NT
+    int a_slot;       // bytes of the activation box slot: [8 * NT rows][256 values] = 4096 * NT
     int stage_bytes;  // bytes per stage (multiple of 1024): weights, activations, gps scale
                       // rows of 256 bytes and, with zero points, gps rows of 64 bytes
     int red_off;      // byte offset of the cluster reduction buffer
@@ -68,7 +67,7 @@ struct Params {
 
 struct StageView {
     uint8_t* w;        // [128 rows][128 B], 128-byte swizzle
-    uint8_t* a;        // 8 x a_slot, each [rows][64 B], 64-byte swizzle
+    uint8_t* a;        // [8 * NT rows][512 B], row-major
     uint16_t* sc;      // [gps][128]
     uint32_t* zp;      // [gps][16]
 };
@@ -77,7 +76,7 @@ __device__ __forceinline__ StageView stage_view(uint8_t* base, const Params& p, 
     StageView v;
     v.w = base + s * p.stage_bytes;
     v.a = v.w + kWBytes;
-    v.sc = reinterpret_cast<uint16_t*>(v.a + 8 * p.a_slot);   // a_slot = 512 * NT
+    v.sc = reinterpret_cast<uint16_t*>(v.a + p.a_slot);
     v.zp = reinterpret_cast<uint32_t*>(v.sc + p.gps * kBN);
     return v;
 }
@@ -93,10 +92,8 @@ __device__ __forceinline__ void load_weights(const StageView& v, const CUtensorM
 }
 
 __device__ __forceinline__ void load_acts(const StageView& v, const CUtensorMap* ta,
-                                          uint64_t* bar, int box, int a_slot) {
-#pragma unroll
-    for (int sub = 0; sub < kBoxK / kSubK; ++sub)
-        tma_load_2d(v.a + sub * a_slot, ta, bar, box * kBoxK + kSubK * sub, 0);
+                                          uint64_t* bar, int box) {
+    tma_load_2d(v.a, ta, bar, box * kBoxK, 0);
 }
 
 // WPG: 32-wide word steps per quantisation group (1, 2, 4 for G = 32, 64, 128);
@@ -109,7 +106,6 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
                                                           const Params p) {
     constexpr int MP = 8 * NT;                      // padded token count of the MMA column tiles
     constexpr int NSETS = NT == 1 ? 2 : 1;          // independent accumulator chains per tile
-    constexpr int kASlot = 512 * NT;                // == p.a_slot: [8 * NT rows][32 values] sub-box
     constexpr int GPB = 8 / WPG;                    // groups per box (1 in the large-group mode)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -147,7 +143,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     if (warp == kConsumerWarps) {
         // ------------------------------ producer ------------------------------
         if (lane == 0) {
-            const uint32_t stage_tx = kWBytes + (kBoxK / kSubK) * uint32_t(p.M) * 64u +
+            const uint32_t stage_tx = kWBytes + uint32_t(p.M) * (kBoxK * 2u) +
                                       uint32_t(p.gps) * kBN * 2u + (ZP ? uint32_t(p.gps) * 64u : 0u);
             tma_prefetch_desc(&tmap_q);
             tma_prefetch_desc(&tmap_a);
@@ -169,7 +165,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
                     mbar_arrive_expect_tx(&full[i], stage_tx);
                     load_weights<ZP>(v, &tmap_q, &tmap_s, &tmap_z, &full[i], b_lo + i, n0, p.g_eff);
                 }
-                load_acts(v, &tmap_a, &full[i], b_lo + i, p.a_slot);
+                load_acts(v, &tmap_a, &full[i], b_lo + i);
             }
             // the next kernel in the stream may start its own prologue now
             grid_launch_dependents();
@@ -180,7 +176,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
                 const StageView v = stage_view(smem, p, s);
                 mbar_arrive_expect_tx(&full[s], stage_tx);
                 load_weights<ZP>(v, &tmap_q, &tmap_s, &tmap_z, &full[s], b_lo + issued, n0, p.g_eff);
-                load_acts(v, &tmap_a, &full[s], b_lo + issued, p.a_slot);
+                load_acts(v, &tmap_a, &full[s], b_lo + issued);
             }
             // copies still in flight must land before the CTA retires
             for (int i = max(0, issued - p.stages); i < issued; ++i)
@@ -233,7 +229,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
             const int tok = 8 * j + g;
-            aoff[j] = tok * 64 + ((t ^ ((tok >> 1) & 3)) << 4);
+            aoff[j] = tok * (kBoxK * 2) + (t << 4);   // K-values 8t .. 8t+7 of the word step
             tok_ok[j] = tok < p.M;
         }
 
@@ -257,9 +253,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
                     unpack_word<BF16>(w1, zc1, q1);
                     const uint32_t a_s0[4] = {q0[0], q1[0], q0[1], q1[1]};
                     const uint32_t a_s1[4] = {q0[2], q1[2], q0[3], q1[3]};
-                    // activation K-values kw + 8t .. +7: sub-box ws, 16-byte chunk t, which
-                    // the 64-byte swizzle places at chunk t ^ ((row / 2) % 4)
-                    const uint8_t* abox = v.a + ws * kASlot;
+                    // activation K-values kw + 8t .. +7 of each token row
+                    const uint8_t* abox = v.a + ws * 64;
 #pragma unroll
                     for (int j = 0; j < NT; ++j) {
                         uint4 b = make_uint4(0u, 0u, 0u, 0u);
@@ -336,12 +331,13 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int tok = 8 * j + 2 * t + (e & 1);
-                const int row = e < 2 ? r0 : r1;
+            for (int h = 0; h < 2; ++h) {   // (row, tokens 2t and 2t+1) as one 8-byte store
+                const int tok = 8 * j + 2 * t;
+                const int row = h == 0 ? r0 : r1;
                 const int owner = row / rows_per;
                 float* dst = cluster.map_shared_rank(red, owner);
-                dst[(rank * rows_per + (row - owner * rows_per)) * MP + tok] = acc[j][e];
+                *reinterpret_cast<float2*>(dst + (rank * rows_per + (row - owner * rows_per)) * MP + tok) =
+                    make_float2(acc[j][2 * h], acc[j][2 * h + 1]);
             }
         }
     }

@@ -212,7 +212,7 @@ w4a16_status launch_decode_path(const void* A, const void* Wq, const void* scale
                   uint64_t(s.ldq) * 4, 32, 128, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st) return st;
     st = make_map(&maps[1], A, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, uint64_t(s.K), uint64_t(s.M),
-                  uint64_t(s.K) * 2, 32, uint32_t(s.M), CU_TENSOR_MAP_SWIZZLE_64B);
+                  uint64_t(s.K) * 2, 256, uint32_t(s.M), CU_TENSOR_MAP_SWIZZLE_NONE);
     if (st) return st;
     st = make_map(&maps[2], scales, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, uint64_t(s.lds), uint64_t(s.ng),
                   uint64_t(s.lds) * 2, 128, gps, CU_TENSOR_MAP_SWIZZLE_NONE);
