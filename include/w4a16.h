@@ -63,8 +63,12 @@ typedef enum { W4A16_FP16 = 0, W4A16_BF16 = 1 } w4a16_dtype;
 typedef enum {
     W4A16_PATH_AUTO = 0,           /* the M-router decides */
     W4A16_PATH_DECODE = 1,         /* small-M split-K kernel (tensor-core mma.sync, M <= 64) */
-    W4A16_PATH_FUSED = 2,          /* fused-dequant tcgen05 GEMM (TMA + TMEM) */
-    W4A16_PATH_DENSE = 3           /* tcgen05 GEMM on a dense dequantised copy */
+    W4A16_PATH_FUSED = 2,          /* fused dequant + tcgen05 GEMM; one of the two below by M */
+    W4A16_PATH_DENSE = 3,          /* tcgen05 GEMM on a dense dequantised copy */
+    W4A16_PATH_FUSED_TMEM = 4,     /* fused, dequantised tile written to tensor memory
+                                      (tcgen05.mma A operand from TMEM; mid M) */
+    W4A16_PATH_FUSED_SMEM = 5      /* fused, dequantised tile written to shared memory
+                                      (both tcgen05.mma operands in SMEM; large M) */
 } w4a16_path;
 
 /*
@@ -160,9 +164,10 @@ w4a16_status w4a16_gemm_ex(const void* A, const void* Wq, const void* scales,
                            int path, void* stream);
 
 /*
- * w4a16_route - the path w4a16_gemm_ex(..., W4A16_PATH_AUTO, ...) takes for
+ * w4a16_route - the kernel w4a16_gemm_ex(..., W4A16_PATH_AUTO, ...) runs for
  * these sizes (has_dense != 0 when a dense copy is supplied).  Host-only.
- * Returns a w4a16_path value (>= 1), or -1 on invalid arguments.
+ * Returns W4A16_PATH_DECODE, _FUSED_TMEM, _FUSED_SMEM or _DENSE, or -1 on
+ * invalid arguments.
  */
 int w4a16_route(int64_t M, int64_t N, int64_t K, int G, int qtype, int dtype, int has_dense);
 

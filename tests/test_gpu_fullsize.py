@@ -65,7 +65,7 @@ def test_zero_point_mlp_pair_full(p):
     x = synth.make_inputs(p)
     C_ref = orc.linear(x.A, x.q, x.scales, x.zeros, p.group_size, p.dtype)
     w = DeviceWeight(p, x.q, x.scales, x.zeros)
-    for path in ("auto", "decode", "fused"):
+    for path in ("auto", "decode", "fused_tmem", "fused_smem"):
         _check(run_gemm(w, x.A, path=path), C_ref, p.dtype, path)
     assert_device_status_ok()
 
@@ -75,7 +75,7 @@ def test_gemv_k512_full():
     x = synth.make_inputs(p)
     C_ref = orc.linear(x.A, x.q, x.scales, x.zeros, p.group_size, p.dtype)
     w = DeviceWeight(p, x.q, x.scales, x.zeros)
-    for path in ("auto", "decode", "fused"):
+    for path in ("auto", "decode", "fused_tmem", "fused_smem"):
         _check(run_gemm(w, x.A, path=path), C_ref, p.dtype, path)
 
 
@@ -90,7 +90,7 @@ def test_prefill_8b_mlp_up_sampled():
     from gpu_helpers import to_host_bits
     # the dense copy itself is bit-exact at full size
     assert np.array_equal(to_host_bits(Wd), W_ref)
-    for path in ("auto", "fused", "dense"):
+    for path in ("auto", "fused_tmem", "fused_smem", "dense"):
         C = run_gemm(w, x.A, path=path, Wdense=Wd if path == "dense" else None)
         _check_sampled(C, ref_rows, ref_pairs, rows, pairs, p.dtype, path)
     assert_device_status_ok()
@@ -122,8 +122,9 @@ def test_crossover_70b_mlp_sampled(sweep_q, ci):
     for M in Ms:
         rows, pairs = _sample(M, p.N, 8, 4096, ci * 100 + M)
         ref_rows, ref_pairs = _sampled_ref(A[:M], W_ref, dt, rows, pairs)
-        C = run_gemm(w, A[:M], path="auto")
-        _check_sampled(C, ref_rows, ref_pairs, rows, pairs, dt, f"M={M}")
+        for path in ("auto", "fused_tmem", "fused_smem"):
+            C = run_gemm(w, A[:M], path=path)
+            _check_sampled(C, ref_rows, ref_pairs, rows, pairs, dt, f"M={M} {path}")
     del w
     torch.cuda.empty_cache()
     assert_device_status_ok()

@@ -76,7 +76,7 @@ def test_dequant_is_bit_exact(cases, sh):
 
 
 def _paths_for(M):
-    paths = ["fused", "dense"]
+    paths = ["fused_tmem", "fused_smem", "dense"]
     if M <= 64:
         paths.insert(0, "decode")
     return paths
@@ -113,7 +113,7 @@ def test_one_hot_activations_return_dequantised_weights_exactly(path, dtype):
     assert np.array_equal(C, w_ref[:, km].T)
 
 
-@pytest.mark.parametrize("path", ["decode", "fused", "dense"])
+@pytest.mark.parametrize("path", ["decode", "fused_tmem", "fused_smem", "dense"])
 def test_integer_valued_gemm_is_exact(path):
     # scale 1, A in {-1, 0, 1}: every partial sum is an integer below 2^24, so the
     # fp32 accumulation is exact in any order and C = rne_dtype(exact).
@@ -157,7 +157,7 @@ def test_outputs_outside_c_are_untouched():
     p = _problem(37, 200, 512, 64, "uint4", "fp16")
     x = synth.make_inputs(p)
     w = DeviceWeight(p, x.q, x.scales, x.zeros)
-    for path in ("decode", "fused"):
+    for path in ("decode", "fused_tmem", "fused_smem"):
         big = torch.full((p.M + 2, p.N), 7.0, dtype=torch.float16, device="cuda")
         C = big[1:-1]
         A = to_dev_bits(x.A, "fp16")

@@ -18,10 +18,11 @@ LIB_PATH = os.path.join(HERE, "libw4a16.so")
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE_TIMEOUT = range(5)
 UINT4B8, UINT4 = 0, 1
 FP16, BF16 = 0, 1
-PATH_AUTO, PATH_DECODE, PATH_FUSED, PATH_DENSE = range(4)
+PATH_AUTO, PATH_DECODE, PATH_FUSED, PATH_DENSE, PATH_FUSED_TMEM, PATH_FUSED_SMEM = range(6)
 QTYPES = {"uint4b8": UINT4B8, "uint4": UINT4}
 DTYPES = {"fp16": FP16, "bf16": BF16}
-PATHS = {"auto": PATH_AUTO, "decode": PATH_DECODE, "fused": PATH_FUSED, "dense": PATH_DENSE}
+PATHS = {"auto": PATH_AUTO, "decode": PATH_DECODE, "fused": PATH_FUSED, "dense": PATH_DENSE,
+         "fused_tmem": PATH_FUSED_TMEM, "fused_smem": PATH_FUSED_SMEM}
 OPT_STATIC_WEIGHTS = 0x100
 
 

@@ -44,6 +44,14 @@ bool plan_decode(int64_t M, int64_t N, int64_t K, int64_t g_eff, int64_t ng, boo
 cudaError_t launch_prefill(const CUtensorMap* maps, void* C, const LayerShape& s, bool dense,
                            int token_tile, cudaStream_t stream);
 
+// tmem_gemm.cu: fused-dequant tcgen05 GEMM with the weight tile in tensor memory.
+// maps: A [M][K] box {64, BT} SW128 (BT = tmem_gemm_token_tile(M)); packed
+// [N][ldq] box {8,128} SW32; scales [ng][lds] box {128,2}; zeros [ng][ldz] box {16,2}.
+int tmem_gemm_token_tile(int64_t M);
+cudaError_t launch_tmem_gemm(const CUtensorMap* maps, void* C, const LayerShape& s, int num_sms,
+                             bool prefetch_weights, cudaStream_t stream);
+int take_status_tmem_gemm();
+
 // Status words of each module: read-and-clear (synchronous).
 int take_status_decode();
 int take_status_prefill();

@@ -1,0 +1,394 @@
+// Fused-dequant W4A16 GEMM with the dequantised weight tile held in tensor memory.
+//
+// Same algebra as the pages' fused kernel (_triton_w4a16_skinny_fmt_kernel:
+// per K step, (q - z).to(dtype) * scale, then a dot with fp32 accumulation),
+// arranged for sm_103a so that no dequantised byte crosses shared memory:
+//
+//   warp 8     weight producer (TMA): per 256-wide K stage, the packed tile
+//              [128 rows x 128 B] (128-byte swizzle) and the scale and zero-point
+//              rows of the groups it spans.  Whole 128-byte row segments keep
+//              DRAM reads in full lines.
+//   warp 10    activation producer (TMA): per 64-wide K block, the tile
+//              [BT tokens x 64] (128-byte swizzle).
+//   warps 0-7  dequantisers: thread = (TMEM lane = weight row, half of a 64-wide
+//              K block); one LOP3 per value pair (magic-number unpack), exact
+//              subtraction of the zero point, one rounding multiply by the scale,
+//              then tcgen05.st of the 16 bf16/fp16 pairs straight into the
+//              block's tensor-memory stage.  They convert block i+1 while the
+//              store of block i drains, and run the epilogue after the K loop.
+//   warp 9     allocates tensor memory; one thread issues
+//              tcgen05.mma.cta_group::1.kind::f16 with A = the weight stage in
+//              TMEM (M = 128 weight rows), B = the activation tile in shared
+//              memory (N = BT tokens), fp32 accumulator in TMEM.
+//
+// Three rings: weight stages (shared memory, released by the dequantisers once
+// read), activation stages (shared memory, released by the MMA) and
+// tensor-memory A stages (32 columns = one 64-wide K block of 128 rows as
+// 16-bit pairs, released by the MMA).  Tensor memory: columns [0, BT) hold the
+// accumulator, every further allocated column an A stage.
+//
+// Small row counts split K over a thread-block cluster (KS CTAs, whole weight
+// stages each): partial accumulators are pushed through distributed shared
+// memory to the CTA that owns each row block and summed there.
+#pragma once
+
+#include <cooperative_groups.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace w4a16 {
+namespace tgemm {
+
+namespace cg = cooperative_groups;
+
+constexpr int kBM = 128;                  // weight rows per CTA (UMMA M, TMEM lanes)
+constexpr int kBK = 64;                   // K per MMA block / activation stage / TMEM stage
+constexpr int kWK = 256;                  // K per weight stage (128 bytes of a packed row)
+constexpr int kSubPerW = kWK / kBK;       // MMA blocks per weight stage
+constexpr int kMaxGps = kWK / 32;         // group rows per weight stage (G >= 32)
+constexpr int kDqWarps = 8;
+constexpr int kWProducerWarp = kDqWarps;
+constexpr int kMmaWarp = kDqWarps + 1;
+constexpr int kAProducerWarp = kDqWarps + 2;
+constexpr int kThreads = (kDqWarps + 3) * 32;
+constexpr int kPkBytes = kBM * kWK / 2;                         // 16 KB packed tile
+constexpr int kScBytes = kMaxGps * kBM * 2;                     // scale rows
+constexpr int kZpBytes = kMaxGps * (kBM / 8) * 4;               // zero-point rows
+constexpr int kWStageBytes = (kPkBytes + kScBytes + kZpBytes + 1023) / 1024 * 1024;
+
+struct Params {
+    uint16_t* C;
+    int* status;
+    int M, N, K, g_eff, ng;
+    int gps;           // group rows per weight stage: min(8, 256 / g_eff), 1 for one group
+    int nkb;           // ceil(K / kBK) MMA blocks
+    int nws;           // ceil(K / kWK) weight stages
+    int ks;            // CTAs per cluster (K split); 1 = whole K per CTA
+    int prefetch_weights;
+};
+
+// Tensor-memory columns per CTA: the accumulator (BT) plus at least two A
+// stages, rounded up to the power of two that tcgen05.alloc takes; every
+// column of the allocation beyond the accumulator holds an A stage.
+constexpr int tmem_cols_for(int bt) {
+    return (bt + 64) <= 128 ? 128 : (bt + 64) <= 256 ? 256 : 512;
+}
+
+// Ring depths per token tile: two CTAs per SM up to BT = 128 (one with the
+// split-K buffer at BT >= 64), 96-128 KB of packed weights in flight per SM.
+template <int BT>
+struct Layout {
+    static constexpr int kWStages = BT <= 32 ? 4 : 3;
+    static constexpr int kAStages = BT <= 16 ? 8 : BT <= 64 ? 4 : 3;
+    static constexpr int kTmemCols = tmem_cols_for(BT);
+    static constexpr int kTmemStages = (kTmemCols - BT) / 32 < 8 ? (kTmemCols - BT) / 32 : 8;
+    static constexpr int kActBytes = BT * kBK * 2;
+    static constexpr int kActOff = kWStages * kWStageBytes;
+    static constexpr int kBarOff = kActOff + kAStages * kActBytes;
+    static constexpr int kRedOff = kBarOff + 512;                 // split-K reduction buffer
+    static constexpr int kRedBytes = kBM * BT * 4;                // [ks][kBM/ks][BT] fp32
+    static constexpr int kBytesNoRed = kRedOff + 1024;
+    static constexpr int kBytesRed = kRedOff + kRedBytes + 1024;
+    static constexpr bool kSplitFits = kBytesRed <= 227 * 1024;
+    static_assert(2 * (kWStages + kAStages + kTmemStages) * 8 + 8 + 4 <= 512, "barrier area");
+};
+
+__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+// D[tmem] (+)= A[tmem] . B[smem desc]^T, kind::f16.
+__device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+template <bool BF16, bool ZP, int BT>
+__global__ void __launch_bounds__(kThreads, 1) tmem_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                                                                const __grid_constant__ CUtensorMap tmap_w,
+                                                                const __grid_constant__ CUtensorMap tmap_s,
+                                                                const __grid_constant__ CUtensorMap tmap_z,
+                                                                const Params p) {
+    using L = Layout<BT>;
+    constexpr int kWStages = L::kWStages;
+    constexpr int kAStages = L::kAStages;
+    constexpr int kTmemStages = L::kTmemStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    auto pk_tile = [&](int s) { return smem + s * kWStageBytes; };
+    auto sc_tile = [&](int s) { return reinterpret_cast<uint16_t*>(pk_tile(s) + kPkBytes); };
+    auto zp_tile = [&](int s) { return reinterpret_cast<uint32_t*>(pk_tile(s) + kPkBytes + kScBytes); };
+    auto act_tile = [&](int s) { return smem + L::kActOff + s * L::kActBytes; };
+    uint64_t* w_full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);   // weight stage landed
+    uint64_t* w_empty = w_full + kWStages;                               // weight stage read
+    uint64_t* a_full = w_empty + kWStages;                               // activation stage landed
+    uint64_t* a_empty = a_full + kAStages;                               // MMA done with it
+    uint64_t* dq_full = a_empty + kAStages;                              // TMEM stage written
+    uint64_t* t_empty = dq_full + kTmemStages;                           // MMA done with it
+    uint64_t* acc_full = t_empty + kTmemStages;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+    float* red = reinterpret_cast<float*>(smem + L::kRedOff);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int rank = p.ks > 1 ? int(blockIdx.x) % p.ks : 0;
+    const int n0 = (p.ks > 1 ? int(blockIdx.x) / p.ks : int(blockIdx.x)) * kBM;
+    const int m0 = blockIdx.y * BT;
+    // this CTA's weight stages [ws_lo, ws_hi) and MMA blocks [kb_lo, kb_hi)
+    const int ws_lo = (rank * p.nws) / p.ks;
+    const int ws_hi = ((rank + 1) * p.nws) / p.ks;
+    const int nws = ws_hi - ws_lo;
+    const int kb_lo = ws_lo * kSubPerW;
+    const int kb_hi = min(ws_hi * kSubPerW, p.nkb);
+    const int nkb = max(kb_hi - kb_lo, 0);
+
+    if (tid == 0) {
+        for (int s = 0; s < kWStages; ++s) {
+            mbar_init(&w_full[s], 1);
+            mbar_init(&w_empty[s], kDqWarps);
+        }
+        for (int s = 0; s < kAStages; ++s) {
+            mbar_init(&a_full[s], 1);
+            mbar_init(&a_empty[s], 1);
+        }
+        for (int t = 0; t < kTmemStages; ++t) {
+            mbar_init(&dq_full[t], kDqWarps);
+            mbar_init(&t_empty[t], 1);
+        }
+        mbar_init(acc_full, 1);
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(tmem_slot, L::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tmem_d = tmem;                 // accumulator columns [0, BT)
+    const uint32_t tmem_a = tmem + BT;            // A stages: 32 columns each
+    bool ok = true;
+
+    if (warp == kWProducerWarp) {
+        // --------------------------- weight producer ---------------------------
+        if (lane == 0) {
+            tma_prefetch_desc(&tmap_w);
+            tma_prefetch_desc(&tmap_s);
+            const uint32_t tx = kPkBytes + uint32_t(p.gps) * (kBM * 2 + (ZP ? (kBM / 8) * 4 : 0));
+            auto load_w = [&](int w) {
+                const int s = w % kWStages, ws = ws_lo + w;
+                const int g0 = (ws * kWK) / p.g_eff;   // first group of the stage
+                mbar_arrive_expect_tx(&w_full[s], tx);
+                tma_load_2d(pk_tile(s), &tmap_w, &w_full[s], ws * (kWK / 8), n0);
+                tma_load_2d(sc_tile(s), &tmap_s, &w_full[s], n0, g0);
+                if constexpr (ZP) tma_load_2d(zp_tile(s), &tmap_z, &w_full[s], n0 / 8, g0);
+            };
+            const int first = min(kWStages, nws);
+            if (!p.prefetch_weights) grid_dependency_wait();
+            for (int w = 0; w < first; ++w) load_w(w);
+            int issued = first;
+            for (; issued < nws; ++issued) {
+                const int s = issued % kWStages;
+                if (!mbar_wait(&w_empty[s], uint32_t(issued / kWStages - 1) & 1u, p.status, 30)) break;
+                load_w(issued);
+            }
+            // no copy may be in flight when the CTA exits
+            for (int w = max(0, issued - kWStages); w < issued; ++w)
+                mbar_wait(&w_full[w % kWStages], uint32_t(w / kWStages) & 1u, p.status, 31);
+        }
+    } else if (warp == kAProducerWarp) {
+        // ------------------------- activation producer -------------------------
+        if (lane == 0) {
+            tma_prefetch_desc(&tmap_a);
+            grid_dependency_wait();   // activations may come from the previous kernel
+            int issued = 0;
+            for (; issued < nkb; ++issued) {
+                const int s = issued % kAStages;
+                if (issued >= kAStages &&
+                    !mbar_wait(&a_empty[s], uint32_t(issued / kAStages - 1) & 1u, p.status, 32))
+                    break;
+                mbar_arrive_expect_tx(&a_full[s], L::kActBytes);
+                tma_load_2d(act_tile(s), &tmap_a, &a_full[s], (kb_lo + issued) * kBK, m0);
+                if (issued == 0) grid_launch_dependents();
+            }
+            if (nkb == 0) grid_launch_dependents();
+            for (int i = max(0, issued - kAStages); i < issued; ++i)
+                mbar_wait(&a_full[i % kAStages], uint32_t(i / kAStages) & 1u, p.status, 33);
+        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------ MMA issuer ------------------------------
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_f16(BF16, kBM, BT);
+            bool good = true;
+            for (int i = 0; i < nkb && good; ++i) {
+                const int s = i % kAStages, t = i % kTmemStages;
+                good = mbar_wait(&a_full[s], uint32_t(i / kAStages) & 1u, p.status, 34) &&
+                       mbar_wait(&dq_full[t], uint32_t(i / kTmemStages) & 1u, p.status, 35);
+                if (!good) break;
+                tc_fence_after();
+                const uint64_t b_desc = smem_desc_sw128(act_tile(s));
+#pragma unroll
+                for (int k = 0; k < kBK / 16; ++k)   // 16 K-values: 8 TMEM columns, 32 smem bytes
+                    umma_f16_ts(tmem_d, tmem_a + uint32_t(32 * t + 8 * k), b_desc + 2 * k, idesc, (i | k) != 0);
+                umma_commit(&a_empty[s]);   // frees the activation stage
+                umma_commit(&t_empty[t]);   // frees the tensor-memory stage
+            }
+            if (good && nkb > 0) umma_commit(acc_full);
+        }
+    } else {
+        // ------------------------------ dequantisers ------------------------------
+        const int row = tid & (kBM - 1);          // TMEM lane / weight row
+        const int half = tid >> 7;                 // K-values 32*half .. +31 of each block
+        const uint32_t lane_base = uint32_t(32 * (warp & 3)) << 16;
+        // group row of a K offset within the stage: group sizes are powers of two
+        // (32 .. 256) or there is one group (shift 31 maps every offset to row 0)
+        const int gshift = p.ng > 1 ? __ffs(p.g_eff) - 1 : 31;
+        // Convert MMA block i (local index) into cols: wait for its weight stage,
+        // read this thread's 16 bytes of the swizzled 128-byte row, release the
+        // stage after its last block.  The 32 K-values lie in one group: every
+        // group size is a multiple of 32, or there is one group.
+        auto convert = [&](int i, uint32_t (&cols)[16]) -> bool {
+            const int w = i / kSubPerW, j = (kb_lo + i) % kSubPerW, s = w % kWStages;
+            if (j == 0 || i == 0)
+                if (!__all_sync(0xffffffffu, mbar_wait(&w_full[s], uint32_t(w / kWStages) & 1u, p.status, 36)))
+                    return false;
+            const int chunk = (2 * j + half) ^ (row & 7);
+            const uint4 wq = *reinterpret_cast<const uint4*>(pk_tile(s) + row * 128 + (chunk << 4));
+            const int gl = (j * kBK + 32 * half) >> gshift;
+            const uint32_t sv = sc_tile(s)[gl * kBM + row];
+            int z = 8;
+            if constexpr (ZP) z = (zp_tile(s)[gl * (kBM / 8) + (row >> 3)] >> (4 * (row & 7))) & 0xF;
+            if (j == kSubPerW - 1 || i == nkb - 1) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&w_empty[s]);
+            }
+            const uint32_t words[4] = {wq.x, wq.y, wq.z, wq.w};
+            const uint32_t s2 = sv | (sv << 16);
+            const ZeroConst zc = make_zero_const<BF16>(z);
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                uint32_t q[4];
+                unpack_word<BF16>(words[jj], zc, q);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) cols[4 * jj + e] = scale_pair<BF16>(q[e], s2);
+            }
+            return true;
+        };
+        uint32_t cols[16], next[16];
+        if (nkb > 0) ok = convert(0, cols);
+        for (int i = 0; i < nkb && ok; ++i) {
+            const int t = i % kTmemStages;
+            // the MMAs that read this tensor-memory stage last time must be complete
+            if (i >= kTmemStages &&
+                !__all_sync(0xffffffffu, mbar_wait(&t_empty[t], uint32_t(i / kTmemStages - 1) & 1u,
+                                                   p.status, 37))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            tmem_st_32x32b_x16(tmem_a + lane_base + uint32_t(32 * t + 16 * half), cols);
+            if (i + 1 < nkb) ok = convert(i + 1, next);   // overlaps the store
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&dq_full[t]);
+#pragma unroll
+            for (int c = 0; c < 16; ++c) cols[c] = next[c];
+        }
+        // ------------------------------ epilogue ------------------------------
+        if (ok && nkb > 0) ok = mbar_wait(acc_full, 0u, p.status, 25);
+        ok = __all_sync(0xffffffffu, ok);
+        tc_fence_after();
+    }
+
+    // Epilogue: warp w reads TMEM lanes 32*(w%4).. and column half w/4 of the tile
+    // (tiles narrower than 32 tokens use warps 0-3 only).
+    constexpr int kHalves = BT >= 32 ? 2 : 1;
+    constexpr int kColsPerWarp = BT / kHalves;
+    const bool epi = warp < 4 * kHalves;
+    const int row = 32 * (warp & 3) + lane;
+    const int c0 = (warp >> 2) * kColsPerWarp;
+    if (p.ks == 1) {
+        if (epi && ok && nkb > 0) {
+            const int n = n0 + row;
+#pragma unroll 1
+            for (int c = 0; c < kColsPerWarp; c += 16) {
+                uint32_t r[16];
+                tmem_ld_32x32b_x16(tmem_d + (uint32_t(32 * (warp & 3)) << 16) + uint32_t(c0 + c), r);
+                tmem_ld_wait();
+                if (n < p.N) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int tok = m0 + c0 + c + j;
+                        if (tok < p.M) p.C[size_t(tok) * p.N + n] = from_f32<BF16>(__uint_as_float(r[j]));
+                    }
+                }
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+        if (warp == kMmaWarp) tmem_dealloc(tmem, L::kTmemCols);
+        return;
+    }
+    // Split K: push the partial tile to the owner of each row block (rows_per rows).
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rows_per = kBM / p.ks;
+    if (epi && ok) {
+        const int owner = row / rows_per;
+        float* dst = cluster.map_shared_rank(red, owner) + (size_t(rank) * rows_per + (row - owner * rows_per)) * BT;
+#pragma unroll 1
+        for (int c = 0; c < kColsPerWarp; c += 16) {
+            uint32_t r[16] = {};   // a CTA without K blocks contributes zeros
+            if (nkb > 0) {
+                tmem_ld_32x32b_x16(tmem_d + (uint32_t(32 * (warp & 3)) << 16) + uint32_t(c0 + c), r);
+                tmem_ld_wait();
+            }
+#pragma unroll
+            for (int j = 0; j < 16; j += 4)
+                *reinterpret_cast<float4*>(dst + c0 + c + j) =
+                    make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
+                                __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+        }
+    }
+    const int any_failed = __syncthreads_or(!ok);
+    cluster.sync();
+    // this CTA owns rows [rank*rows_per, (rank+1)*rows_per) of the tile
+    const int items = rows_per * BT;
+    for (int it = tid; it < items; it += kThreads) {
+        const int rl = it % rows_per, col = it / rows_per;
+        float sum = 0.f;
+        for (int c = 0; c < p.ks; ++c) sum += red[(size_t(c) * rows_per + rl) * BT + col];
+        const int n = n0 + rank * rows_per + rl, tok = m0 + col;
+        if (n < p.N && tok < p.M && !any_failed) p.C[size_t(tok) * p.N + n] = from_f32<BF16>(sum);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) tmem_dealloc(tmem, L::kTmemCols);
+}
+
+}  // namespace tgemm
+}  // namespace w4a16

@@ -29,6 +29,9 @@ w4a16_status fail(w4a16_status code, const char* fmt, ...) {
 }
 
 w4a16_status cuda_fail(cudaError_t e, const char* what) {
+    // A failed launch also leaves the error in the runtime's per-thread "last
+    // error"; clear it so that it is not reported again by a later, unrelated call.
+    (void)cudaGetLastError();
     return fail(W4A16_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
 }
 
@@ -141,11 +144,16 @@ w4a16_status device_sms(int* sms) {
 }
 
 // --- router -----------------------------------------------------------------
-// Crossover points measured on GB300 (decode kernel vs fused tcgen05 kernel);
-// the dense copy wins over fused dequant only where the tensor pipe, not the
-// dequantisation, limits the fused kernel.
-constexpr int64_t kDecodeUpToM = 32;
+// Crossover points measured on GB300 (decode kernel vs the two fused tcgen05
+// kernels); the dense copy wins over fused dequant only where the tensor pipe,
+// not the dequantisation, limits the fused kernel.
+constexpr int64_t kDecodeUpToM = 16;
+constexpr int64_t kTmemUpToM = 128;
 constexpr int64_t kDenseFromM = 1024;
+
+int fused_kernel_for(int64_t M) {
+    return M <= kTmemUpToM ? W4A16_PATH_FUSED_TMEM : W4A16_PATH_FUSED_SMEM;
+}
 
 int route_impl(const LayerShape& s, bool has_dense) {
     const int64_t M = s.M;
@@ -156,7 +164,7 @@ int route_impl(const LayerShape& s, bool has_dense) {
             return W4A16_PATH_DECODE;
     }
     if (has_dense && M >= kDenseFromM) return W4A16_PATH_DENSE;
-    return W4A16_PATH_FUSED;
+    return fused_kernel_for(M);
 }
 
 int token_tile_for(int64_t M) {
@@ -197,6 +205,37 @@ w4a16_status launch_tcgen05(const void* A, const void* Wsrc, bool dense, const v
     }
     cudaError_t e = launch_prefill(maps, C, s, dense, bt, stream);
     if (e != cudaSuccess) return cuda_fail(e, "tcgen05 GEMM launch");
+    return W4A16_OK;
+}
+
+w4a16_status launch_tmem_path(const void* A, const void* Wq, const void* scales,
+                              const int32_t* zeros, void* C, const LayerShape& s,
+                              bool static_weights, cudaStream_t stream) {
+    int sms = 0;
+    w4a16_status st = device_sms(&sms);
+    if (st) return st;
+    const int bt = tmem_gemm_token_tile(s.M);
+    // weight stages of 256 K-values: 128-byte packed rows and the group rows they span
+    const uint32_t gps = uint32_t(decode_scale_box_rows(s.g_eff, s.ng));
+    CUtensorMap maps[4];
+    st = make_map(&maps[0], A, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, uint64_t(s.K), uint64_t(s.M),
+                  uint64_t(s.K) * 2, 64, uint32_t(bt), CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st) return st;
+    st = make_map(&maps[1], Wq, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, uint64_t(s.ldq), uint64_t(s.N),
+                  uint64_t(s.ldq) * 4, 32, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st) return st;
+    st = make_map(&maps[2], scales, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, uint64_t(s.lds), uint64_t(s.ng),
+                  uint64_t(s.lds) * 2, 128, gps, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (st) return st;
+    if (s.zp) {
+        st = make_map(&maps[3], zeros, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, uint64_t(s.ldz),
+                      uint64_t(s.ng), uint64_t(s.ldz) * 4, 16, gps, CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (st) return st;
+    } else {
+        maps[3] = maps[2];   // unused without zero points
+    }
+    cudaError_t e = launch_tmem_gemm(maps, C, s, sms, static_weights, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "tensor-memory GEMM launch");
     return W4A16_OK;
 }
 
@@ -298,7 +337,7 @@ w4a16_status w4a16_gemm_ex(const void* A, const void* Wq, const void* scales,
     const int opts = path & ~0xFF;
     path &= 0xFF;
     if (opts & ~W4A16_OPT_STATIC_WEIGHTS) return fail(W4A16_ERR_INVALID_ARG, "unknown option bits 0x%x", opts);
-    if (path < W4A16_PATH_AUTO || path > W4A16_PATH_DENSE) return fail(W4A16_ERR_INVALID_ARG, "unknown path %d", path);
+    if (path < W4A16_PATH_AUTO || path > W4A16_PATH_FUSED_SMEM) return fail(W4A16_ERR_INVALID_ARG, "unknown path %d", path);
     st = check_qptrs(Wq, scales, zeros, qtype);
     if (st) return st;
     if (!A || !aligned(A, 16)) return fail(W4A16_ERR_INVALID_ARG, "A must be a non-null 16-byte aligned device pointer");
@@ -306,6 +345,7 @@ w4a16_status w4a16_gemm_ex(const void* A, const void* Wq, const void* scales,
     if (Wdense && !aligned(Wdense, 16)) return fail(W4A16_ERR_INVALID_ARG, "Wdense must be 16-byte aligned");
     s.M = M;
     if (path == W4A16_PATH_AUTO) path = route_impl(s, Wdense != nullptr);
+    if (path == W4A16_PATH_FUSED) path = fused_kernel_for(M);
     if (path == W4A16_PATH_DENSE && !Wdense) return fail(W4A16_ERR_INVALID_ARG, "the dense path needs a dense copy (Wdense)");
     if (path == W4A16_PATH_DECODE) {
         int ks, stages, nt;
@@ -320,7 +360,8 @@ w4a16_status w4a16_gemm_ex(const void* A, const void* Wq, const void* scales,
     if (path == W4A16_PATH_DECODE)
         return launch_decode_path(A, Wq, scales, zeros, C, s, (opts & W4A16_OPT_STATIC_WEIGHTS) != 0, cs);
     if (path == W4A16_PATH_DENSE) return launch_tcgen05(A, Wdense, true, nullptr, nullptr, C, s, cs);
-    return launch_tcgen05(A, Wq, false, scales, zeros, C, s, cs);
+    if (path == W4A16_PATH_FUSED_SMEM) return launch_tcgen05(A, Wq, false, scales, zeros, C, s, cs);
+    return launch_tmem_path(A, Wq, scales, zeros, C, s, (opts & W4A16_OPT_STATIC_WEIGHTS) != 0, cs);
 }
 
 w4a16_status w4a16_gemm(const void* A, const void* Wq, const void* scales, const int32_t* zeros,
@@ -376,6 +417,7 @@ w4a16_status w4a16_device_status(int* site) {
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
     int v = take_status_decode();
     if (v == 0) v = take_status_prefill();
+    if (v == 0) v = take_status_tmem_gemm();
     if (site) *site = v > 0 ? v : 0;
     if (v < 0) return fail(W4A16_ERR_CUDA, "reading the device status word failed");
     if (v > 0) return fail(W4A16_ERR_DEVICE_TIMEOUT, "a kernel barrier wait timed out at site %d", v);
