@@ -65,7 +65,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true", help="skip the prefill/zero-point side measurements")
-    ap.add_argument("--profile-case", choices=["decode", "decode_large", "zp", "prefill", "dense", "dequant"],
+    ap.add_argument("--profile-case", choices=["decode", "decode_large", "zp", "mid", "prefill", "prefill_smem", "dense", "dequant"],
                     help="only run `--reps` eager launches of one kernel (for ncu), then exit")
     ap.add_argument("--reps", type=int, default=8)
     return ap.parse_args()
@@ -323,7 +323,7 @@ def extras(torch, B, synth, peaks):
         for i, (_, wq, sp, _) in enumerate(lay):
             B.gemm_ex(A, wq, sp, None, dense[i] if path == "dense" else None, Cs[i], M, N, K, G,
                       "uint4b8", "bf16", path)
-    for path in ("fused", "dense"):
+    for path in ("fused_tmem", "fused_smem", "dense"):
         t = time_graph(torch, lambda: run(path), 10, 3) / len(lay)
         out[f"prefill_{path}_m2048_k4096_n14336"] = {
             "tflops": flops / t / 1e12, "us": t * 1e6,
@@ -369,10 +369,11 @@ def profile_case(args):
     from w4a16_int4_weight_gb300 import inputs as synth
     tdt = torch.bfloat16
     c = args.profile_case
-    if c in ("decode", "decode_large", "zp"):
+    if c in ("decode", "decode_large", "zp", "mid"):
         M, N, K, G, qt = {"decode": (8, N_, K_, G_, QTYPE),
                           "decode_large": (1, 28672, 8192, 64, QTYPE),
-                          "zp": (16, 11008, 4096, 32, "uint4")}[c]
+                          "zp": (16, 11008, 4096, 32, "uint4"),
+                          "mid": (64, 28672, 8192, 64, QTYPE)}[c]
         lay = make_layers(torch, B, synth, 4, M, N, K, G, qt, "bf16")
         A = torch.randn(M, K, device="cuda").to(tdt)
         C = torch.empty(M, N, dtype=tdt, device="cuda")
@@ -392,7 +393,7 @@ def profile_case(args):
                 B.dequant(wq, sp, None, W, N, K, G, "uint4b8", "bf16")
             else:
                 B.gemm_ex(A, wq, sp, None, W if c == "dense" else None, C, M, N, K, G, "uint4b8",
-                          "bf16", "dense" if c == "dense" else "fused")
+                          "bf16", {"dense": "dense", "prefill": "fused_tmem", "prefill_smem": "fused_smem"}[c])
     torch.cuda.synchronize()
     code, site = B.device_status()
     print(f"profile case {c}: {args.reps} launches, device status {code}")

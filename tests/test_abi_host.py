@@ -102,14 +102,14 @@ def test_pack_and_dequant_validation(B):
 
 
 def test_router(B):
-    # small M -> decode; mid M -> fused with the tile in tensor memory; large M ->
-    # fused with the tile in shared memory; dense copy used only for large M
+    # small M -> decode; larger M -> fused with the tile in tensor memory; dense
+    # copy used only for large M
     assert B.route(1, 4096, 4096, 128, "uint4b8", "bf16") == B.PATH_DECODE
     assert B.route(16, 11008, 4096, 32, "uint4", "bf16") == B.PATH_DECODE
     assert B.route(17, 28672, 8192, 64, "uint4b8", "fp16") == B.PATH_FUSED_TMEM
     assert B.route(128, 28672, 8192, 64, "uint4", "bf16") == B.PATH_FUSED_TMEM
-    assert B.route(129, 28672, 8192, 64, "uint4", "bf16") == B.PATH_FUSED_SMEM
-    assert B.route(2048, 14336, 4096, 128, "uint4b8", "bf16") == B.PATH_FUSED_SMEM
+    assert B.route(129, 28672, 8192, 64, "uint4", "bf16") == B.PATH_FUSED_TMEM
+    assert B.route(2048, 14336, 4096, 128, "uint4b8", "bf16") == B.PATH_FUSED_TMEM
     assert B.route(2048, 14336, 4096, 128, "uint4b8", "bf16", has_dense=True) == B.PATH_DENSE
     assert B.route(4, 14336, 4096, 128, "uint4b8", "bf16", has_dense=True) == B.PATH_DECODE
     assert B.route(4, 14336, 4100, 128, "uint4b8", "bf16") == -1

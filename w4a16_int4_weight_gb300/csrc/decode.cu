@@ -45,58 +45,72 @@ int decode_scale_box_rows(int64_t g_eff, int64_t ng) {
     return int(decode::kBoxK / g_eff);
 }
 
-// Host-side plan for a shape: cluster size (K split), ring depth, shared memory.
-// K is split over up to 8 CTAs until there are about three CTAs per SM.  Each
-// ring stage holds one 256-wide K box.
+// Host-side plan for a shape: cluster size ks (K split) and ring depth, from a
+// cost model fitted to a grid of GB300 timings (N 4096..28672, K 2048..14336,
+// M 1 and 16, every ks and depth; the model's choice is within 3% of the best
+// measured plan on average, 10% at worst):
+//   work      boxes on the busiest SM: ceil(CTAs / SMs) * boxes per CTA;
+//   waves     CTAs beyond what fits on the GPU at once (20% per extra wave);
+//   in flight weight bytes requested ahead per SM (up to 10% below 64 KB);
+//   room      small layers run best when the next kernel's CTAs fit beside
+//             this one's, so that their weight prefetch (PDL) overlaps it
+//             (60% when they do not fit, for <= 12 boxes per SM);
+//   one CTA   a lone CTA per SM hides latency worse (20%);
+//   split     each doubling of ks costs 3% (reduction).
 bool plan_decode(int64_t M, int64_t N, int64_t K, int64_t g_eff, int64_t ng, bool zp,
                  int num_sms, int* ks_out, int* stages_out, size_t* smem_out, int* nt_out) {
     using namespace decode;
-    if (M < 1 || M > kDecodeMaxM) return false;
+    if (M < 1 || M > kDecodeMaxM || num_sms < 1) return false;
     const int nt = M <= 8 ? 1 : M <= 16 ? 2 : M <= 32 ? 4 : 8;
     const int64_t row_tiles = (N + kBN - 1) / kBN;
     const int64_t nboxes = (K + kBoxK - 1) / kBoxK;
-    const int64_t target = 3LL * num_sms;
-    int ks = 1;
-    while (ks < 8 && row_tiles * ks < target && 2 * ks <= nboxes) ks *= 2;
-    const int64_t boxes_per = (nboxes + ks - 1) / ks;
     const int sb = stage_bytes_for(M, decode_scale_box_rows(g_eff, ng), zp);
-    const size_t red = ks > 1 ? size_t(kBN) * 8 * nt * 4 : 0;
-    auto smem_for = [&](int s) { return size_t(s) * sb + 128 + red + 1024; };
-    const size_t sm_bytes = 228 * 1024;
     const int max_ctas = nt == 1 ? 4 : nt == 2 ? 3 : 1;   // register limit of the instantiations
-    // Pick the depth: at least ~96 KB of weight boxes in flight per SM (enough to
-    // cover HBM latency at full bandwidth), then as many resident CTAs (consumer
-    // warps) as possible, then the shallowest ring.
-    int best = 1;
-    long best_ctas = -1, best_inflight = -1;
-    bool best_ok = false;
-    for (int s = 1; s <= kMaxStages && s <= boxes_per; ++s) {
-        const size_t sm = smem_for(s);
-        if (sm > 227 * 1024) break;
-        long ctas = long(sm_bytes / (sm + 1024));
-        if (ctas > max_ctas) ctas = max_ctas;
-        const long ahead = s == boxes_per ? s : s - 1;
-        const long inflight = ctas * ahead * kWBytes;
-        const bool ok = inflight >= 96 * 1024;
-        const bool better = ok ? (!best_ok || ctas > best_ctas) : (!best_ok && inflight > best_inflight);
-        if (better) {
-            best = s;
-            best_ctas = ctas;
-            best_inflight = inflight;
-            best_ok = ok;
+    constexpr int kMaxPlanStages = 5;                       // the range the model was fitted on
+    double best_cost = 0.0;
+    int best_ks = 0, best_st = 0;
+    size_t best_smem = 0;
+    for (int ks = 1; ks <= 8 && ks <= nboxes; ks *= 2) {
+        const int64_t ctas = row_tiles * ks;
+        const int64_t per = (ctas + num_sms - 1) / num_sms;
+        const int64_t bp = (nboxes + ks - 1) / ks;
+        const size_t red = ks > 1 ? size_t(kBN) * 8 * nt * 4 : 0;
+        for (int st = 1; st <= kMaxPlanStages; ++st) {
+            if (st > bp && st > 1) break;
+            const size_t smem = size_t(st) * sb + 128 + red + 1024;
+            if (smem > 227 * 1024) break;
+            int64_t r = int64_t(228 * 1024) / int64_t(smem + 1024);
+            if (r > max_ctas) r = max_ctas;
+            if (r < 1) break;
+            const int64_t waves = (per + r - 1) / r;
+            const int64_t ahead = st == 1 ? 1 : (st < bp ? st - 1 : bp);
+            const double inflight_kb = double(per < r ? per : r) * double(ahead) * 16.0;
+            const double work = double(per * bp);
+            double cost = work * (1.0 + 0.2 * double(waves - 1));
+            if (inflight_kb < 64.0) cost *= 1.0 + 0.1 * (64.0 - inflight_kb) / 64.0;
+            if (work <= 12.0 && r - per < per) cost *= 1.6;
+            if (per == 1) cost *= 1.2;
+            int lg = 0;
+            for (int k = ks; k > 1; k >>= 1) ++lg;
+            cost *= 1.0 + 0.03 * lg;
+            // ties: smaller split, then deeper ring
+            if (best_ks == 0 || cost < best_cost - 1e-9) {
+                best_cost = cost;
+                best_ks = ks;
+                best_st = st;
+                best_smem = smem;
+            } else if (cost <= best_cost + 1e-9 && ks == best_ks && st > best_st) {
+                best_st = st;
+                best_smem = smem;
+            }
         }
     }
-    for (int stages = best; stages >= 1; --stages) {
-        const size_t smem = smem_for(stages);
-        if (smem <= 227 * 1024) {
-            *ks_out = ks;
-            *stages_out = stages;
-            *smem_out = smem;
-            *nt_out = nt;
-            return true;
-        }
-    }
-    return false;
+    if (best_ks == 0) return false;
+    *ks_out = best_ks;
+    *stages_out = best_st;
+    *smem_out = best_smem;
+    *nt_out = nt;
+    return true;
 }
 
 cudaError_t launch_decode(const CUtensorMap* maps, void* C, const LayerShape& s, int num_sms,

@@ -144,16 +144,16 @@ w4a16_status device_sms(int* sms) {
 }
 
 // --- router -----------------------------------------------------------------
-// Crossover points measured on GB300 (decode kernel vs the two fused tcgen05
-// kernels); the dense copy wins over fused dequant only where the tensor pipe,
-// not the dequantisation, limits the fused kernel.
+// Crossover points measured on GB300 (decode kernel vs the fused tcgen05
+// kernels): decode wins up to M = 16 on every measured layer.  The fused kernel
+// with the dequantised tile in tensor memory beats the one with both operands
+// in shared memory at every measured M (1 .. 2048); the latter stays reachable
+// as W4A16_PATH_FUSED_SMEM.  The dense copy wins over fused dequant only where
+// the tensor pipe, not the dequantisation, limits the fused kernel.
 constexpr int64_t kDecodeUpToM = 16;
-constexpr int64_t kTmemUpToM = 128;
 constexpr int64_t kDenseFromM = 1024;
 
-int fused_kernel_for(int64_t M) {
-    return M <= kTmemUpToM ? W4A16_PATH_FUSED_TMEM : W4A16_PATH_FUSED_SMEM;
-}
+int fused_kernel_for(int64_t) { return W4A16_PATH_FUSED_TMEM; }
 
 int route_impl(const LayerShape& s, bool has_dense) {
     const int64_t M = s.M;
