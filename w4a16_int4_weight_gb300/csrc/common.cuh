@@ -252,18 +252,20 @@ struct ZeroConst {
     uint32_t hi;   // fp16 only: pair added after the 1/16 scaling, -(64 + z)
 };
 
+// Bit patterns built with integer operations (z in 0..15, all values exact):
+//   bf16 128 + z     = 0x4300 + z        (ulp 1 in [128, 256))
+//   fp16 1024 + z    = 0x6400 + z        (ulp 1 in [1024, 2048))
+//   fp16 -(64 + z)   = 0xD400 + 16 z     (ulp 1/16 in [64, 128))
 template <bool BF16>
 __device__ __forceinline__ ZeroConst make_zero_const(int z) {
     ZeroConst c;
+    const uint32_t u = uint32_t(z) & 0xFu;
     if constexpr (BF16) {
-        __nv_bfloat16 v = __float2bfloat16_rn(128.0f + float(z));
-        c.lo = as_u32(__nv_bfloat162(v, v));
+        c.lo = (0x4300u | u) * 0x00010001u;
         c.hi = 0;
     } else {
-        __half v = __float2half_rn(1024.0f + float(z));
-        __half u = __float2half_rn(-(64.0f + float(z)));
-        c.lo = as_u32(__half2(v, v));
-        c.hi = as_u32(__half2(u, u));
+        c.lo = (0x6400u | u) * 0x00010001u;
+        c.hi = (0xD400u | (u << 4)) * 0x00010001u;
     }
     return c;
 }

@@ -68,12 +68,11 @@ struct Params {
     int prefetch_weights;
 };
 
-// Tensor-memory columns per CTA: the accumulator (BT) plus at least two A
-// stages, rounded up to the power of two that tcgen05.alloc takes; every
-// column of the allocation beyond the accumulator holds an A stage.
-constexpr int tmem_cols_for(int bt) {
-    return (bt + 64) <= 128 ? 128 : (bt + 64) <= 256 ? 256 : 512;
-}
+// Tensor-memory columns per CTA (a power of two for tcgen05.alloc): the
+// accumulator (BT) and a power-of-two number of 32-column A stages, four up to
+// BT = 128 (two CTAs per SM share the 512 columns) and eight at BT = 256.
+constexpr int tmem_cols_for(int bt) { return bt <= 128 ? 256 : 512; }
+constexpr int tmem_stages_for(int bt) { return bt <= 128 ? 4 : 8; }
 
 // Ring depths per token tile: two CTAs per SM up to BT = 128 (one with the
 // split-K buffer at BT >= 64), 96-128 KB of packed weights in flight per SM.
@@ -82,7 +81,10 @@ struct Layout {
     static constexpr int kWStages = BT <= 32 ? 4 : 3;
     static constexpr int kAStages = BT <= 16 ? 8 : BT <= 64 ? 4 : 3;
     static constexpr int kTmemCols = tmem_cols_for(BT);
-    static constexpr int kTmemStages = (kTmemCols - BT) / 32 < 8 ? (kTmemCols - BT) / 32 : 8;
+    static constexpr int kTmemStages = tmem_stages_for(BT);
+    static_assert(BT + 32 * kTmemStages <= kTmemCols, "tensor-memory budget");
+    static_assert(kTmemStages >= kSubPerW && (kTmemStages & (kTmemStages - 1)) == 0,
+                  "a weight stage's blocks map to consecutive tensor-memory stages");
     static constexpr int kActBytes = BT * kBK * 2;
     static constexpr int kActOff = kWStages * kWStageBytes;
     static constexpr int kBarOff = kActOff + kAStages * kActBytes;
@@ -261,34 +263,34 @@ __global__ void __launch_bounds__(kThreads, 1) tmem_gemm_kernel(const __grid_con
         }
     } else {
         // ------------------------------ dequantisers ------------------------------
-        const int row = tid & (kBM - 1);          // TMEM lane / weight row
-        const int half = tid >> 7;                 // K-values 32*half .. +31 of each block
-        const uint32_t lane_base = uint32_t(32 * (warp & 3)) << 16;
-        // group row of a K offset within the stage: group sizes are powers of two
-        // (32 .. 256) or there is one group (shift 31 maps every offset to row 0)
-        const int gshift = p.ng > 1 ? __ffs(p.g_eff) - 1 : 31;
-        // Convert MMA block i (local index) into cols: wait for its weight stage,
-        // read this thread's 16 bytes of the swizzled 128-byte row, release the
-        // stage after its last block.  The 32 K-values lie in one group: every
+        // Thread = (weight row = TMEM lane, half of each 64-wide block).  One
+        // weight stage (4 blocks) per iteration, block index j a compile-time
+        // constant, so per-thread offsets are precomputed and no register array
+        // is copied.  The 32 K-values of a (row, half) lie in one group: every
         // group size is a multiple of 32, or there is one group.
-        auto convert = [&](int i, uint32_t (&cols)[16]) -> bool {
-            const int w = i / kSubPerW, j = (kb_lo + i) % kSubPerW, s = w % kWStages;
-            if (j == 0 || i == 0)
-                if (!__all_sync(0xffffffffu, mbar_wait(&w_full[s], uint32_t(w / kWStages) & 1u, p.status, 36)))
-                    return false;
-            const int chunk = (2 * j + half) ^ (row & 7);
-            const uint4 wq = *reinterpret_cast<const uint4*>(pk_tile(s) + row * 128 + (chunk << 4));
+        const int row = tid & (kBM - 1);
+        const int half = tid >> 7;
+        const uint32_t t_addr = tmem_a + (uint32_t(32 * (warp & 3)) << 16) + uint32_t(16 * half);
+        const int gshift = p.ng > 1 ? __ffs(p.g_eff) - 1 : 31;   // 31: one group
+        int pk_off[kSubPerW], sc_off[kSubPerW], zp_off[kSubPerW];
+#pragma unroll
+        for (int j = 0; j < kSubPerW; ++j) {
+            pk_off[j] = row * 128 + (((2 * j + half) ^ (row & 7)) << 4);
             const int gl = (j * kBK + 32 * half) >> gshift;
-            const uint32_t sv = sc_tile(s)[gl * kBM + row];
+            sc_off[j] = gl * kBM + row;
+            zp_off[j] = gl * (kBM / 8) + (row >> 3);
+        }
+        const int zp_shift = 4 * (row & 7);
+        uint32_t ca[16], cb[16];
+        auto convert = [&](const uint8_t* stg, int j, uint32_t (&cols)[16]) {
+            const uint4 wq = *reinterpret_cast<const uint4*>(stg + pk_off[j]);
+            const uint32_t sv = reinterpret_cast<const uint16_t*>(stg + kPkBytes)[sc_off[j]];
+            const uint32_t s2 = __byte_perm(sv, 0u, 0x1010);
             int z = 8;
-            if constexpr (ZP) z = (zp_tile(s)[gl * (kBM / 8) + (row >> 3)] >> (4 * (row & 7))) & 0xF;
-            if (j == kSubPerW - 1 || i == nkb - 1) {
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&w_empty[s]);
-            }
-            const uint32_t words[4] = {wq.x, wq.y, wq.z, wq.w};
-            const uint32_t s2 = sv | (sv << 16);
+            if constexpr (ZP)
+                z = int(reinterpret_cast<const uint32_t*>(stg + kPkBytes + kScBytes)[zp_off[j]] >> zp_shift);
             const ZeroConst zc = make_zero_const<BF16>(z);
+            const uint32_t words[4] = {wq.x, wq.y, wq.z, wq.w};
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) {
                 uint32_t q[4];
@@ -296,28 +298,58 @@ __global__ void __launch_bounds__(kThreads, 1) tmem_gemm_kernel(const __grid_con
 #pragma unroll
                 for (int e = 0; e < 4; ++e) cols[4 * jj + e] = scale_pair<BF16>(q[e], s2);
             }
-            return true;
         };
-        uint32_t cols[16], next[16];
-        if (nkb > 0) ok = convert(0, cols);
-        for (int i = 0; i < nkb && ok; ++i) {
-            const int t = i % kTmemStages;
-            // the MMAs that read this tensor-memory stage last time must be complete
-            if (i >= kTmemStages &&
-                !__all_sync(0xffffffffu, mbar_wait(&t_empty[t], uint32_t(i / kTmemStages - 1) & 1u,
-                                                   p.status, 37))) {
-                ok = false;
-                break;
-            }
+        // hand block (stage w, index j) to the MMA: wait for its TMEM stage to be
+        // free, store, and signal
+        auto store = [&](int w, int j, const uint32_t (&cols)[16]) -> bool {
+            const int li = w * kSubPerW + j;
+            const int t = li & (kTmemStages - 1);
+            if (li >= kTmemStages &&
+                !__all_sync(0xffffffffu, mbar_wait(&t_empty[t], uint32_t(li / kTmemStages + 1) & 1u,
+                                                   p.status, 37)))
+                return false;
             tc_fence_after();
-            tmem_st_32x32b_x16(tmem_a + lane_base + uint32_t(32 * t + 16 * half), cols);
-            if (i + 1 < nkb) ok = convert(i + 1, next);   // overlaps the store
+            tmem_st_32x32b_x16(t_addr + uint32_t(32 * t), cols);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&dq_full[t]);
+            return true;
+        };
+        for (int w = 0; w < nws && ok; ++w) {
+            const int s = w % kWStages;
+            if (!__all_sync(0xffffffffu, mbar_wait(&w_full[s], uint32_t(w / kWStages) & 1u, p.status, 36))) {
+                ok = false;
+                break;
+            }
+            const uint8_t* stg = pk_tile(s);
+            const int nj = min(kSubPerW, nkb - w * kSubPerW);
+            if (nj == kSubPerW) {
+                // converting block j + 1 overlaps the store of block j
+                convert(stg, 0, ca);
+                convert(stg, 1, cb);
+                ok = store(w, 0, ca);
+                convert(stg, 2, ca);
+                ok = ok && store(w, 1, cb);
+                convert(stg, 3, cb);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&w_empty[s]);   // the stage has been read
+                ok = ok && store(w, 2, ca);
+                ok = ok && store(w, 3, cb);
+            } else {
+                // the last stage of a K range that ends inside it
 #pragma unroll
-            for (int c = 0; c < 16; ++c) cols[c] = next[c];
+                for (int j = 0; j < kSubPerW; ++j) {
+                    if (j < nj) {
+                        convert(stg, j, ca);
+                        if (j == nj - 1) {
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&w_empty[s]);
+                        }
+                        ok = ok && store(w, j, ca);
+                    }
+                }
+            }
         }
         // ------------------------------ epilogue ------------------------------
         if (ok && nkb > 0) ok = mbar_wait(acc_full, 0u, p.status, 25);
