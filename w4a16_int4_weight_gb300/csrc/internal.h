@@ -46,7 +46,8 @@ cudaError_t launch_prefill(const CUtensorMap* maps, void* C, const LayerShape& s
 
 // tmem_gemm.cu: fused-dequant tcgen05 GEMM with the weight tile in tensor memory.
 // maps: A [M][K] box {64, BT} SW128 (BT = tmem_gemm_token_tile(M)); packed
-// [N][ldq] box {8,128} SW32; scales [ng][lds] box {128,2}; zeros [ng][ldz] box {16,2}.
+// [N][ldq] box {32,128} SW128; scales [ng][lds] box {128, gps}; zeros [ng][ldz]
+// box {16, gps}, gps = decode_scale_box_rows(g_eff, ng).
 int tmem_gemm_token_tile(int64_t M);
 cudaError_t launch_tmem_gemm(const CUtensorMap* maps, void* C, const LayerShape& s, int num_sms,
                              bool prefetch_weights, cudaStream_t stream);

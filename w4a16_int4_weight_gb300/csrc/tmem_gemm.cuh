@@ -128,8 +128,13 @@ __device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
         : "memory");
 }
 
+// CTAs per SM the register budget must allow (the launch plan assumes two up
+// to BT = 128).  Three thinner CTAs per SM at BT <= 64 (two weight and two A
+// stages) and splitting 128/256-token tiles over clusters both measured slower.
+constexpr int min_ctas_for(int bt) { return bt <= 128 ? 2 : 1; }
+
 template <bool BF16, bool ZP, int BT>
-__global__ void __launch_bounds__(kThreads, 1) tmem_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
+__global__ void __launch_bounds__(kThreads, min_ctas_for(BT)) tmem_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                                                 const __grid_constant__ CUtensorMap tmap_w,
                                                                 const __grid_constant__ CUtensorMap tmap_s,
                                                                 const __grid_constant__ CUtensorMap tmap_z,
