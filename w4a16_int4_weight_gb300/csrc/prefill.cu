@@ -84,8 +84,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int n0 = blockIdx.x * kBM;
-    const int m0 = blockIdx.y * BT;
+    // token tiles vary fastest, so the CTAs that share a weight tile run together
+    // and read it from L2 after the first
+    const int tiles_m = (p.M + BT - 1) / BT;
+    const int n0 = int(blockIdx.x / tiles_m) * kBM;
+    const int m0 = int(blockIdx.x % tiles_m) * BT;
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -236,7 +239,9 @@ cudaError_t launch_t(const CUtensorMap* maps, const Params& p, cudaStream_t stre
     constexpr int smem = Layout<BT, DENSE>::kBytes;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    dim3 grid((p.N + kBM - 1) / kBM, (p.M + BT - 1) / BT);
+    const int64_t ctas = int64_t((p.N + kBM - 1) / kBM) * ((p.M + BT - 1) / BT);
+    if (ctas > int64_t(0x7fffffff)) return cudaErrorInvalidValue;   // beyond any C that fits in memory
+    const dim3 grid(static_cast<unsigned>(ctas));
     kern<<<grid, kThreads, smem, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
     return cudaGetLastError();
 }

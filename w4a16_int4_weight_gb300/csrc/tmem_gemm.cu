@@ -146,8 +146,10 @@ cudaError_t launch_tmem_gemm(const CUtensorMap* maps, void* C, const LayerShape&
     p.ks = tmem_gemm_ksplit(s.M, s.N, s.K, num_sms);
     p.prefetch_weights = prefetch_weights ? 1 : 0;
     const int bt = tmem_gemm_token_tile(s.M);
-    const int gx = int((s.N + tgemm::kBM - 1) / tgemm::kBM) * p.ks;
-    const int gy = int((s.M + bt - 1) / bt);
+    const int64_t ctas = ((s.N + tgemm::kBM - 1) / tgemm::kBM) * ((s.M + bt - 1) / bt) * p.ks;
+    if (ctas > int64_t(0x7fffffff)) return cudaErrorInvalidValue;   // beyond any C that fits in memory
+    const int gx = int(ctas);
+    const int gy = 1;
     switch (bt) {
         case 16: return launch_bt<16>(maps, p, s.bf16, s.zp, gx, gy, stream);
         case 32: return launch_bt<32>(maps, p, s.bf16, s.zp, gx, gy, stream);

@@ -161,9 +161,14 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BT)) tmem_gemm_kernel(c
     float* red = reinterpret_cast<float*>(smem + L::kRedOff);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // blockIdx.x = (n tile * token tiles + token tile) * ks + rank: the ks CTAs of
+    // a cluster are consecutive, and token tiles vary fastest so that the CTAs
+    // sharing a weight tile run together and read it from L2 after the first
+    const int tiles_m = (p.M + BT - 1) / BT;
     const int rank = p.ks > 1 ? int(blockIdx.x) % p.ks : 0;
-    const int n0 = (p.ks > 1 ? int(blockIdx.x) / p.ks : int(blockIdx.x)) * kBM;
-    const int m0 = blockIdx.y * BT;
+    const int tile = p.ks > 1 ? int(blockIdx.x) / p.ks : int(blockIdx.x);
+    const int n0 = (tile / tiles_m) * kBM;
+    const int m0 = (tile % tiles_m) * BT;
     // this CTA's weight stages [ws_lo, ws_hi) and MMA blocks [kb_lo, kb_hi)
     const int ws_lo = (rank * p.nws) / p.ks;
     const int ws_hi = ((rank + 1) * p.nws) / p.ks;
