@@ -258,8 +258,9 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BT)) tmem_gemm_kernel(c
             bool good = true;
             for (int i = 0; i < nkb && good; ++i) {
                 const int s = i % kAStages, t = i % kTmemStages;
-                good = mbar_wait(&a_full[s], uint32_t(i / kAStages) & 1u, p.status, 34) &&
-                       mbar_wait(&dq_full[t], uint32_t(i / kTmemStages) & 1u, p.status, 35);
+                // dq_full completes only after dequant warp 0 has seen the block's
+                // activation tile land (a_full), so one wait covers both
+                good = mbar_wait(&dq_full[t], uint32_t(i / kTmemStages) & 1u, p.status, 35);
                 if (!good) break;
                 tc_fence_after();
                 const uint64_t b_desc = smem_desc_sw128(act_tile(s));
@@ -322,6 +323,11 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BT)) tmem_gemm_kernel(c
             tmem_st_32x32b_x16(t_addr + uint32_t(32 * t), cols);
             tmem_st_wait();
             tc_fence_before();
+            // warp 0 signals only once the block's activation tile has landed
+            if (warp == 0 &&
+                !__all_sync(0xffffffffu, mbar_wait(&a_full[li % kAStages], uint32_t(li / kAStages) & 1u,
+                                                   p.status, 34)))
+                return false;
             __syncwarp();
             if (lane == 0) mbar_arrive(&dq_full[t]);
             return true;
