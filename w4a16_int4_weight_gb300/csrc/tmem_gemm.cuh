@@ -78,22 +78,28 @@ constexpr int tmem_stages_for(int bt) { return bt <= 128 ? 4 : 8; }
 // split-K buffer at BT >= 64), 96-128 KB of packed weights in flight per SM.
 template <int BT>
 struct Layout {
+    // The MMA issuer takes K blocks in units of kUnit: one wait and two commits
+    // per unit.  At N <= 64 every M=128, K=16 MMA costs ~45 cycles whatever N, so
+    // pairing blocks there halves the issuer's fixed cost per block.
+    static constexpr int kUnit = BT <= 64 ? 2 : 1;
     static constexpr int kWStages = BT <= 32 ? 4 : 3;
-    static constexpr int kAStages = BT <= 16 ? 8 : BT <= 64 ? 4 : 3;
+    static constexpr int kAUnits = BT <= 16 ? 4 : BT <= 64 ? 2 : 3;   // activation unit-slots
     static constexpr int kTmemCols = tmem_cols_for(BT);
-    static constexpr int kTmemStages = tmem_stages_for(BT);
+    static constexpr int kTmemStages = tmem_stages_for(BT);           // 32-column block stages
+    static constexpr int kTUnits = kTmemStages / kUnit;               // tensor-memory unit-slots
     static_assert(BT + 32 * kTmemStages <= kTmemCols, "tensor-memory budget");
-    static_assert(kTmemStages >= kSubPerW && (kTmemStages & (kTmemStages - 1)) == 0,
-                  "a weight stage's blocks map to consecutive tensor-memory stages");
-    static constexpr int kActBytes = BT * kBK * 2;
+    static_assert((kTmemStages & (kTmemStages - 1)) == 0, "power-of-two tensor-memory ring");
+    static_assert(kSubPerW % kUnit == 0 && kTUnits >= 2, "units tile a weight stage");
+    static constexpr int kActBytes = BT * kBK * 2;                    // one activation tile
+    static constexpr int kAUnitBytes = kUnit * kActBytes;
     static constexpr int kActOff = kWStages * kWStageBytes;
-    static constexpr int kBarOff = kActOff + kAStages * kActBytes;
+    static constexpr int kBarOff = kActOff + kAUnits * kAUnitBytes;
     static constexpr int kRedOff = kBarOff + 512;                 // split-K reduction buffer
     static constexpr int kRedBytes = kBM * BT * 4;                // [ks][kBM/ks][BT] fp32
     static constexpr int kBytesNoRed = kRedOff + 1024;
     static constexpr int kBytesRed = kRedOff + kRedBytes + 1024;
     static constexpr bool kSplitFits = kBytesRed <= 227 * 1024;
-    static_assert(2 * (kWStages + kAStages + kTmemStages) * 8 + 8 + 4 <= 512, "barrier area");
+    static_assert(2 * (kWStages + kAUnits + kTUnits) * 8 + 8 + 4 <= 512, "barrier area");
 };
 
 __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
@@ -141,22 +147,26 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BT)) tmem_gemm_kernel(c
                                                                 const Params p) {
     using L = Layout<BT>;
     constexpr int kWStages = L::kWStages;
-    constexpr int kAStages = L::kAStages;
+    constexpr int kUnit = L::kUnit;
+    constexpr int kAUnits = L::kAUnits;
     constexpr int kTmemStages = L::kTmemStages;
+    constexpr int kTUnits = L::kTUnits;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
     auto pk_tile = [&](int s) { return smem + s * kWStageBytes; };
     auto sc_tile = [&](int s) { return reinterpret_cast<uint16_t*>(pk_tile(s) + kPkBytes); };
     auto zp_tile = [&](int s) { return reinterpret_cast<uint32_t*>(pk_tile(s) + kPkBytes + kScBytes); };
-    auto act_tile = [&](int s) { return smem + L::kActOff + s * L::kActBytes; };
+    auto act_tile = [&](int slot, int g) {
+        return smem + L::kActOff + slot * L::kAUnitBytes + g * L::kActBytes;
+    };
     uint64_t* w_full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);   // weight stage landed
     uint64_t* w_empty = w_full + kWStages;                               // weight stage read
-    uint64_t* a_full = w_empty + kWStages;                               // activation stage landed
-    uint64_t* a_empty = a_full + kAStages;                               // MMA done with it
-    uint64_t* dq_full = a_empty + kAStages;                              // TMEM stage written
-    uint64_t* t_empty = dq_full + kTmemStages;                           // MMA done with it
-    uint64_t* acc_full = t_empty + kTmemStages;
+    uint64_t* a_full = w_empty + kWStages;                               // activation unit landed
+    uint64_t* a_empty = a_full + kAUnits;                                // MMA done with it
+    uint64_t* dq_full = a_empty + kAUnits;                               // TMEM unit written
+    uint64_t* t_empty = dq_full + kTUnits;                               // MMA done with it
+    uint64_t* acc_full = t_empty + kTUnits;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
     float* red = reinterpret_cast<float*>(smem + L::kRedOff);
 
@@ -176,17 +186,18 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BT)) tmem_gemm_kernel(c
     const int kb_lo = ws_lo * kSubPerW;
     const int kb_hi = min(ws_hi * kSubPerW, p.nkb);
     const int nkb = max(kb_hi - kb_lo, 0);
+    const int nunits = (nkb + kUnit - 1) / kUnit;                     // MMA units of kUnit blocks
 
     if (tid == 0) {
         for (int s = 0; s < kWStages; ++s) {
             mbar_init(&w_full[s], 1);
             mbar_init(&w_empty[s], kDqWarps);
         }
-        for (int s = 0; s < kAStages; ++s) {
+        for (int s = 0; s < kAUnits; ++s) {
             mbar_init(&a_full[s], 1);
             mbar_init(&a_empty[s], 1);
         }
-        for (int t = 0; t < kTmemStages; ++t) {
+        for (int t = 0; t < kTUnits; ++t) {
             mbar_init(&dq_full[t], kDqWarps);
             mbar_init(&t_empty[t], 1);
         }
@@ -238,37 +249,48 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BT)) tmem_gemm_kernel(c
             tma_prefetch_desc(&tmap_a);
             grid_dependency_wait();   // activations may come from the previous kernel
             int issued = 0;
-            for (; issued < nkb; ++issued) {
-                const int s = issued % kAStages;
-                if (issued >= kAStages &&
-                    !mbar_wait(&a_empty[s], uint32_t(issued / kAStages - 1) & 1u, p.status, 32))
+            for (; issued < nunits; ++issued) {
+                const int s = issued % kAUnits;
+                if (issued >= kAUnits &&
+                    !mbar_wait(&a_empty[s], uint32_t(issued / kAUnits - 1) & 1u, p.status, 32))
                     break;
-                mbar_arrive_expect_tx(&a_full[s], L::kActBytes);
-                tma_load_2d(act_tile(s), &tmap_a, &a_full[s], (kb_lo + issued) * kBK, m0);
+                const int nb = min(kUnit, nkb - kUnit * issued);
+                mbar_arrive_expect_tx(&a_full[s], uint32_t(nb * L::kActBytes));
+                for (int g = 0; g < nb; ++g)
+                    tma_load_2d(act_tile(s, g), &tmap_a, &a_full[s], (kb_lo + kUnit * issued + g) * kBK, m0);
                 if (issued == 0) grid_launch_dependents();
             }
-            if (nkb == 0) grid_launch_dependents();
-            for (int i = max(0, issued - kAStages); i < issued; ++i)
-                mbar_wait(&a_full[i % kAStages], uint32_t(i / kAStages) & 1u, p.status, 33);
+            if (nunits == 0) grid_launch_dependents();
+            for (int u = max(0, issued - kAUnits); u < issued; ++u)
+                mbar_wait(&a_full[u % kAUnits], uint32_t(u / kAUnits) & 1u, p.status, 33);
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------ MMA issuer ------------------------------
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f16(BF16, kBM, BT);
             bool good = true;
-            for (int i = 0; i < nkb && good; ++i) {
-                const int s = i % kAStages, t = i % kTmemStages;
-                // dq_full completes only after dequant warp 0 has seen the block's
-                // activation tile land (a_full), so one wait covers both
-                good = mbar_wait(&dq_full[t], uint32_t(i / kTmemStages) & 1u, p.status, 35);
+            for (int u = 0; u < nunits && good; ++u) {
+                const int s = u % kAUnits, tu = u % kTUnits;
+                // dq_full completes only after dequant warp 0 has seen the unit's
+                // activation tiles land (a_full), so one wait covers both
+                good = mbar_wait(&dq_full[tu], uint32_t(u / kTUnits) & 1u, p.status, 35);
                 if (!good) break;
                 tc_fence_after();
-                const uint64_t b_desc = smem_desc_sw128(act_tile(s));
+                const int nb = min(kUnit, nkb - kUnit * u);
 #pragma unroll
-                for (int k = 0; k < kBK / 16; ++k)   // 16 K-values: 8 TMEM columns, 32 smem bytes
-                    umma_f16_ts(tmem_d, tmem_a + uint32_t(32 * t + 8 * k), b_desc + 2 * k, idesc, (i | k) != 0);
-                umma_commit(&a_empty[s]);   // frees the activation stage
-                umma_commit(&t_empty[t]);   // frees the tensor-memory stage
+                for (int g = 0; g < kUnit; ++g) {
+                    if (g < nb) {
+                        const int i = kUnit * u + g;                  // block, TMEM stage i % T
+                        const uint32_t a_col = uint32_t(32 * (i & (kTmemStages - 1)));
+                        const uint64_t b_desc = smem_desc_sw128(act_tile(s, g));
+#pragma unroll
+                        for (int k = 0; k < kBK / 16; ++k)   // 16 K-values: 8 TMEM columns, 32 smem bytes
+                            umma_f16_ts(tmem_d, tmem_a + a_col + uint32_t(8 * k), b_desc + 2 * k, idesc,
+                                        (i | k) != 0);
+                    }
+                }
+                umma_commit(&a_empty[s]);    // frees the activation unit
+                umma_commit(&t_empty[tu]);   // frees the tensor-memory unit
             }
             if (good && nkb > 0) umma_commit(acc_full);
         }
@@ -310,27 +332,29 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BT)) tmem_gemm_kernel(c
                 for (int e = 0; e < 4; ++e) cols[4 * jj + e] = scale_pair<BF16>(q[e], s2);
             }
         };
-        // hand block (stage w, index j) to the MMA: wait for its TMEM stage to be
-        // free, store, and signal
-        auto store = [&](int w, int j, const uint32_t (&cols)[16]) -> bool {
-            const int li = w * kSubPerW + j;
-            const int t = li & (kTmemStages - 1);
-            if (li >= kTmemStages &&
-                !__all_sync(0xffffffffu, mbar_wait(&t_empty[t], uint32_t(li / kTmemStages + 1) & 1u,
-                                                   p.status, 37)))
-                return false;
-            tc_fence_after();
-            tmem_st_32x32b_x16(t_addr + uint32_t(32 * t), cols);
+        // Hand-off of MMA unit u (blocks kUnit*u ..): before its first store, wait
+        // until the MMAs that last read its tensor-memory slot are complete; after
+        // its last store, wait for the stores, and (warp 0) for the unit's
+        // activation tiles, then signal the issuer.
+        auto unit_free = [&](int u) -> bool {
+            const int tu = u % kTUnits;
+            return u < kTUnits ||
+                   __all_sync(0xffffffffu, mbar_wait(&t_empty[tu], uint32_t(u / kTUnits + 1) & 1u, p.status, 37));
+        };
+        auto unit_done = [&](int u) -> bool {
             tmem_st_wait();
             tc_fence_before();
-            // warp 0 signals only once the block's activation tile has landed
             if (warp == 0 &&
-                !__all_sync(0xffffffffu, mbar_wait(&a_full[li % kAStages], uint32_t(li / kAStages) & 1u,
-                                                   p.status, 34)))
+                !__all_sync(0xffffffffu, mbar_wait(&a_full[u % kAUnits], uint32_t(u / kAUnits) & 1u, p.status, 34)))
                 return false;
             __syncwarp();
-            if (lane == 0) mbar_arrive(&dq_full[t]);
+            if (lane == 0) mbar_arrive(&dq_full[u % kTUnits]);
             return true;
+        };
+        // block li (local index) into its 32-column tensor-memory stage
+        auto put = [&](int li, const uint32_t (&cols)[16]) {
+            tc_fence_after();
+            tmem_st_32x32b_x16(t_addr + uint32_t(32 * (li & (kTmemStages - 1))), cols);
         };
         for (int w = 0; w < nws && ok; ++w) {
             const int s = w % kWStages;
@@ -339,30 +363,63 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BT)) tmem_gemm_kernel(c
                 break;
             }
             const uint8_t* stg = pk_tile(s);
-            const int nj = min(kSubPerW, nkb - w * kSubPerW);
-            if (nj == kSubPerW) {
-                // converting block j + 1 overlaps the store of block j
+            const int b0 = w * kSubPerW;                        // first block of the stage
+            const int nj = min(kSubPerW, nkb - b0);
+            if (nj == kSubPerW && kUnit == 2) {
+                // units (0,1) and (2,3) of the stage
+                const int u0 = b0 / 2;
                 convert(stg, 0, ca);
                 convert(stg, 1, cb);
-                ok = store(w, 0, ca);
+                ok = unit_free(u0);
+                if (ok) {
+                    put(b0, ca);
+                    put(b0 + 1, cb);
+                    ok = unit_done(u0);
+                }
                 convert(stg, 2, ca);
-                ok = ok && store(w, 1, cb);
                 convert(stg, 3, cb);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&w_empty[s]);   // the stage has been read
-                ok = ok && store(w, 2, ca);
-                ok = ok && store(w, 3, cb);
+                ok = ok && unit_free(u0 + 1);
+                if (ok) {
+                    put(b0 + 2, ca);
+                    put(b0 + 3, cb);
+                    ok = unit_done(u0 + 1);
+                }
+            } else if (nj == kSubPerW) {
+                // one block per unit: block j + 1 is converted before block j is handed off
+                auto hand = [&](int li, const uint32_t (&cols)[16]) -> bool {
+                    if (!unit_free(li)) return false;
+                    put(li, cols);
+                    return unit_done(li);
+                };
+                convert(stg, 0, ca);
+                convert(stg, 1, cb);
+                ok = hand(b0, ca);
+                convert(stg, 2, ca);
+                ok = ok && hand(b0 + 1, cb);
+                convert(stg, 3, cb);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&w_empty[s]);
+                ok = ok && hand(b0 + 2, ca);
+                ok = ok && hand(b0 + 3, cb);
             } else {
                 // the last stage of a K range that ends inside it
 #pragma unroll
                 for (int j = 0; j < kSubPerW; ++j) {
                     if (j < nj) {
+                        const int li = b0 + j, u = li / kUnit;
                         convert(stg, j, ca);
                         if (j == nj - 1) {
                             __syncwarp();
                             if (lane == 0) mbar_arrive(&w_empty[s]);
                         }
-                        ok = ok && store(w, j, ca);
+                        if (li % kUnit == 0) ok = ok && unit_free(u);
+                        if (ok) {
+                            put(li, ca);
+                            tmem_st_wait();   // ca is reused by the next block
+                        }
+                        if (li % kUnit == kUnit - 1 || j == nj - 1) ok = ok && unit_done(u);
                     }
                 }
             }
