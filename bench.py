@@ -483,6 +483,27 @@ def main():
                          "tflops": 2.0 * M * N_ * K_ / t / 1e12,
                          "frac_of_hbm": alg_bytes(M, N_, K_, G_, False) / t / 1e9 / hbm_peak}
 
+    # spread of single steps: 200 graph replays, each between its own events
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(200)]
+    for a, b in evs:
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    step_ms = sorted(a.elapsed_time(b) for a, b in evs)
+    step_spread = {"steps": len(step_ms), "p10_ms": step_ms[len(step_ms) // 10],
+                   "p50_ms": step_ms[len(step_ms) // 2], "p90_ms": step_ms[(9 * len(step_ms)) // 10]}
+
+    # hot L2: one layer's weights (8.4 MB, resident in L2) called LAYERS times per M
+    hot_l2 = {}
+    for M in MS:
+        def hot_m(M=M):
+            _, wq, sp, _ = layers[0]
+            for l in range(LAYERS):
+                gemm(M, l, wq, sp)
+        t = time_graph(torch, hot_m, 300, 10) / LAYERS
+        hot_l2[str(M)] = {"us_per_launch": t * 1e6, "alg_gbs": alg_bytes(M, N_, K_, G_, False) / t / 1e9}
+
     # ---- end to end through the C ABI: host activations in, host outputs out ----
     A_pin = {M: A_host[M].pin_memory() for M in MS}
     C_pin = {M: torch.empty(LAYERS, M, N_, dtype=tdt).pin_memory() for M in MS}
@@ -549,6 +570,8 @@ def main():
             "tflops": world * args.steps * flops_step / t_max / 1e12,
             "alg_gbs": world * args.steps * abytes_step / t_max / 1e9,
             "per_m": per_m,
+            "step_spread": step_spread,
+            "hot_l2": hot_l2,
             "gpu_launches": args.steps * launches_per_step,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                          "frac": achieved / hbm_peak, "traffic": traffic,

@@ -70,6 +70,7 @@ def _load():
             "orc_gemm_rows": (None, [P, P, P, I64, I64, I64, I, P]),
             "orc_gemm_pairs": (None, [P, P, P, P, I64, I64, I, P]),
             "orc_linear_rows": (I, [P, P, I64, P, P, P, I64, I64, I64, I64, I, P]),
+            "orc_add_bias": (None, [P, I64, I64, P, I]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -188,9 +189,20 @@ def gemm_pairs(A, W, ms, ns, dtype: str) -> np.ndarray:
     return out
 
 
-def linear(A, q, scales, zeros, group_size: int, dtype: str) -> np.ndarray:
-    """The whole layer from unpacked q: dequant then float64 GEMM."""
-    return gemm(A, dequant(q, scales, zeros, group_size, dtype), dtype)
+def add_bias(C: np.ndarray, bias, dtype: str) -> np.ndarray:
+    """C[m,n] + bias[n] in float64 (bias given as dtype bits [N]); returns a new array."""
+    out = np.array(C, dtype=np.float64, order="C", copy=True)
+    b = _c(bias, np.uint16)
+    M, N = out.shape
+    assert b.shape == (N,)
+    _load().orc_add_bias(_ptr(out), M, N, _ptr(b), DTYPE_CODE[dtype])
+    return out
+
+
+def linear(A, q, scales, zeros, group_size: int, dtype: str, bias=None) -> np.ndarray:
+    """The whole layer from unpacked q: dequant, float64 GEMM, then + bias[n] if given."""
+    C = gemm(A, dequant(q, scales, zeros, group_size, dtype), dtype)
+    return C if bias is None else add_bias(C, bias, dtype)
 
 
 def linear_rows_packed(A, words, K: int, scales, zeros, rows, group_size: int,

@@ -241,6 +241,14 @@ void orc_gemm_pairs(const uint16_t* A, const uint16_t* W, const int64_t* ms, con
     }
 }
 
+/* Bias: C[m][n] += bias[n] (dtype bits), the value the pages add to the GEMM
+ * output ("rdna_hybrid_w4a16", _rdna_hybrid_w4a16_apply_impl: the bias vector
+ * of the linear layer, one value per output feature n).  C stays in float64. */
+void orc_add_bias(double* C, int64_t M, int64_t N, const uint16_t* bias, int dtype) {
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) C[m * N + n] += dt_value(bias[n], dtype);
+}
+
 /* The whole layer in the pages' order on a packed weight: unpack -> dequant ->
  * GEMM over the selected rows of A.  Used as the timed CPU baseline. */
 int orc_linear_rows(const uint16_t* A, const uint32_t* words, int64_t ldq, const uint16_t* scales,

@@ -362,3 +362,47 @@ def test_inputs_are_seeded_and_in_range():
     with np.errstate(over="ignore"):
         first = _mix64(np.array([key0 + GOLDEN_GAMMA], dtype=np.uint64))[0]
     assert int(first) == 0xE220A8397B1DCDAF
+
+
+# --------------------------------------------------------------------------
+# Bias (one value per output feature n, added to the GEMM output)
+# --------------------------------------------------------------------------
+
+def test_bias_hand_case():
+    # M=2, N=3, K=16, uint4b8, G=-1, scale 0.25 everywhere, A = one-hot rows.
+    # w[n][k] = (q - 8) * 0.25; row m of A selects k = 3 (m=0) and k = 9 (m=1).
+    # q[n][3] = 10, 6, 8 -> w = 0.5, -0.5, 0; q[n][9] = 12, 8, 0 -> w = 1, 0, -2.
+    # bias = (0.25, -1.5, 3): C = [[0.75, -2.0, 3.0], [1.25, -1.5, 1.0]] exactly.
+    q = np.full((3, 16), 8, dtype=np.uint8)
+    q[:, 3] = [10, 6, 8]
+    q[:, 9] = [12, 8, 0]
+    s = np.full((3, 1), 0x3E80, dtype=np.uint16)          # bf16 0.25
+    A = np.zeros((2, 16), dtype=np.uint16)
+    A[0, 3] = 0x3F80                                         # 1.0
+    A[1, 9] = 0x3F80
+    bias = np.array([0x3E80, 0xBFC0, 0x4040], dtype=np.uint16)   # 0.25, -1.5, 3.0
+    C = orc.linear(A, q, s, None, -1, "bf16", bias=bias)
+    assert np.array_equal(C, np.array([[0.75, -2.0, 3.0], [1.25, -1.5, 1.0]]))
+
+
+def test_bias_with_zero_weights_is_the_bias():
+    p = synth.Problem(5, 40, 64, 32, "uint4", "fp16")
+    _, s, z = synth.make_weights(p)
+    # every q equal to its row's zero point: w = 0 exactly
+    q = np.empty((40, 64), dtype=np.uint8)
+    for n in range(40):
+        for g in range(2):
+            q[n, 32 * g:32 * (g + 1)] = orc.zero_point(z, 2, n, g)
+    A = synth.make_activations(p)
+    bias = orc.round_to(np.linspace(-3, 3, 40), "fp16")
+    C = orc.linear(A, q, s, z, 32, "fp16", bias=bias)
+    assert np.array_equal(C, np.broadcast_to(orc.values(bias, "fp16"), (5, 40)))
+
+
+def test_bias_is_added_per_output_feature():
+    p = synth.Problem(6, 24, 128, 64, "uint4b8", "bf16")
+    x = synth.make_inputs(p)
+    bias = orc.round_to(np.arange(24, dtype=np.float64) * 0.125 - 1.0, "bf16")
+    C0 = orc.linear(x.A, x.q, x.scales, None, 64, "bf16")
+    C1 = orc.linear(x.A, x.q, x.scales, None, 64, "bf16", bias=bias)
+    assert np.allclose(C1 - C0, np.broadcast_to(orc.values(bias, "bf16"), C0.shape), rtol=0, atol=1e-12)
