@@ -164,6 +164,23 @@ w4a16_status w4a16_gemm_ex(const void* A, const void* Wq, const void* scales,
                            int path, void* stream);
 
 /*
+ * w4a16_linear - the linear layer with its bias: C[m,n] = rne_dtype(sum_k
+ * A[m,k] * w[n,k] + bias[n]), the bias of the pages' apply path
+ * (rdna_hybrid_w4a16, _rdna_hybrid_w4a16_apply_impl: a per-output-feature
+ * vector, handed to the skinny kernel or added to the fused GEMM's output).
+ * Here it is added to the fp32 accumulator in every kernel's epilogue, so the
+ * output is rounded once (the pages' fused path adds it after rounding, in
+ * the dtype: two roundings; both lie within the GEMM tolerance).
+ *   bias     device dtype [N], 2-byte aligned, or NULL for none.
+ *   Every other argument, the validation and the error behaviour are those of
+ *   w4a16_gemm_ex, which is w4a16_linear with bias NULL.
+ */
+w4a16_status w4a16_linear(const void* A, const void* Wq, const void* scales,
+                          const int32_t* zeros, const void* bias, const void* Wdense, void* C,
+                          int64_t M, int64_t N, int64_t K, int G, int qtype, int dtype, int path,
+                          void* stream);
+
+/*
  * w4a16_route - the kernel w4a16_gemm_ex(..., W4A16_PATH_AUTO, ...) runs for
  * these sizes (has_dense != 0 when a dense copy is supplied).  Host-only.
  * Returns W4A16_PATH_DECODE, _FUSED_TMEM, _FUSED_SMEM or _DENSE, or -1 on

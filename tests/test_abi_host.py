@@ -125,3 +125,9 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     mod = importlib.util.module_from_spec(spec)
     with pytest.raises(ImportError, match="not built"):
         spec.loader.exec_module(mod)
+
+
+def test_linear_rejects_a_misaligned_bias(B):
+    code = B.lib.w4a16_linear(FAKE, FAKE, FAKE, None, FAKE + 1, None, FAKE, 4, 256, 4096, 128, 0, 1, 0, None)
+    assert code == B.ERR_INVALID_ARG
+    assert "bias" in B.last_error()

@@ -50,6 +50,7 @@ _SIGS = {
     "w4a16_pack": (_I, [_P, _P, _P, _P, _I64, _I64, _I, _I, _I, _P]),
     "w4a16_gemm": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _P]),
     "w4a16_gemm_ex": (_I, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _I, _P]),
+    "w4a16_linear": (_I, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _I, _P]),
     "w4a16_route": (_I, [_I64, _I64, _I64, _I, _I, _I, _I]),
     "w4a16_dequant": (_I, [_P, _P, _P, _P, _I64, _I64, _I, _I, _I, _P]),
     "w4a16_gemm_dense": (_I, [_P, _P, _P, _I64, _I64, _I64, _I, _P]),
@@ -138,6 +139,16 @@ def gemm_ex(A, Wq, scales, zeros, Wdense, C, M, N, K, G, qtype, dtype, path="aut
         p |= OPT_STATIC_WEIGHTS
     _check(lib.w4a16_gemm_ex(_ptr(A), _ptr(Wq), _ptr(scales), _ptr(zeros), _ptr(Wdense),
                              _ptr(C), M, N, K, G, _qt(qtype), _dt(dtype), p, _stream(stream)))
+
+
+def linear(A, Wq, scales, zeros, bias, Wdense, C, M, N, K, G, qtype, dtype, path="auto",
+           stream=None, static_weights=False):
+    """gemm_ex plus bias[N] (dtype) added before the output rounding; bias may be None."""
+    p = PATHS[path] if isinstance(path, str) else int(path)
+    if static_weights:
+        p |= OPT_STATIC_WEIGHTS
+    _check(lib.w4a16_linear(_ptr(A), _ptr(Wq), _ptr(scales), _ptr(zeros), _ptr(bias), _ptr(Wdense),
+                            _ptr(C), M, N, K, G, _qt(qtype), _dt(dtype), p, _stream(stream)))
 
 
 def route(M, N, K, G, qtype, dtype, has_dense=False) -> int:

@@ -113,8 +113,8 @@ bool plan_decode(int64_t M, int64_t N, int64_t K, int64_t g_eff, int64_t ng, boo
     return true;
 }
 
-cudaError_t launch_decode(const CUtensorMap* maps, void* C, const LayerShape& s, int num_sms,
-                          bool prefetch_weights, cudaStream_t stream) {
+cudaError_t launch_decode(const CUtensorMap* maps, void* C, const void* bias, const LayerShape& s,
+                          int num_sms, bool prefetch_weights, cudaStream_t stream) {
     using namespace decode;
     int ks, stages, nt;
     size_t smem;
@@ -122,6 +122,7 @@ cudaError_t launch_decode(const CUtensorMap* maps, void* C, const LayerShape& s,
         return cudaErrorInvalidValue;
     Params p;
     p.C = static_cast<uint16_t*>(C);
+    p.bias = static_cast<const uint16_t*>(bias);
     p.status = status_ptr();
     if (!p.status) return cudaErrorSymbolNotFound;
     p.M = int(s.M);

@@ -52,6 +52,7 @@ constexpr int kMaxGps = 8;               // groups per box at G = 32
 
 struct Params {
     uint16_t* C;
+    const uint16_t* bias;   // [N] dtype, added before the final rounding; may be null
     int* status;      // device status word (first timed-out wait site)
     int M, N, K, g_eff;
     int nboxes;       // ceil(K / kBoxK)
@@ -308,15 +309,19 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
 
     // C fragment: (row g, tokens 2t, 2t+1) and (row g + 8, same tokens)
     const bool consumer = warp < kConsumerWarps;
+    // the bias of an output row, 0 without one
+    auto bias_of = [&](int n) { return p.bias && n < p.N ? to_f32<BF16>(p.bias[n]) : 0.f; };
     if (p.ks == 1) {
         if (consumer && !failed) {
+            const float b0 = bias_of(n0 + r0), b1 = bias_of(n0 + r1);
 #pragma unroll
             for (int j = 0; j < NT; ++j) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int tok = 8 * j + 2 * t + (e & 1);
                     const int n = n0 + (e < 2 ? r0 : r1);
-                    if (tok < p.M && n < p.N) p.C[size_t(tok) * p.N + n] = from_f32<BF16>(acc[j][e]);
+                    if (tok < p.M && n < p.N)
+                        p.C[size_t(tok) * p.N + n] = from_f32<BF16>(acc[j][e] + (e < 2 ? b0 : b1));
                 }
             }
         }
@@ -349,7 +354,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
         float sum = 0.f;
         for (int c = 0; c < p.ks; ++c) sum += red[(c * rows_per + rl) * MP + tok];
         const int n = n0 + rank * rows_per + rl;
-        if (n < p.N && !any_failed) p.C[size_t(tok) * p.N + n] = from_f32<BF16>(sum);
+        if (n < p.N && !any_failed) p.C[size_t(tok) * p.N + n] = from_f32<BF16>(sum + bias_of(n));
     }
 }
 

@@ -32,8 +32,9 @@ constexpr int64_t kDecodeMaxM = 64;
 // scales [ng][lds] box {128, decode_scale_box_rows}; zeros [ng][ldz] box {16, same}.
 // prefetch_weights: the weights are not written by work still running on the
 // stream, so they may be fetched before the previous grid completes.
-cudaError_t launch_decode(const CUtensorMap* maps, void* C, const LayerShape& s, int num_sms,
-                          bool prefetch_weights, cudaStream_t stream);
+// bias (all three GEMMs): [N] dtype added to the fp32 result before its rounding, or null.
+cudaError_t launch_decode(const CUtensorMap* maps, void* C, const void* bias, const LayerShape& s,
+                          int num_sms, bool prefetch_weights, cudaStream_t stream);
 int decode_scale_box_rows(int64_t g_eff, int64_t ng);
 bool plan_decode(int64_t M, int64_t N, int64_t K, int64_t g_eff, int64_t ng, bool zp,
                  int num_sms, int* ks_out, int* stages_out, size_t* smem_out, int* nt_out);
@@ -41,7 +42,7 @@ bool plan_decode(int64_t M, int64_t N, int64_t K, int64_t g_eff, int64_t ng, boo
 // prefill.cu: tcgen05 GEMM, fused-dequant (Wq != null) or dense (tmap_w dense).
 // maps: A [M][K] box {64,BT} SW128; weights (packed [N][ldq] box {8,128} SW32, or
 // dense [N][K] box {64,128} SW128); scales [ng][lds] box {128,2}; zeros [ng][ldz] box {16,2}.
-cudaError_t launch_prefill(const CUtensorMap* maps, void* C, const LayerShape& s, bool dense,
+cudaError_t launch_prefill(const CUtensorMap* maps, void* C, const void* bias, const LayerShape& s, bool dense,
                            int token_tile, cudaStream_t stream);
 
 // tmem_gemm.cu: fused-dequant tcgen05 GEMM with the weight tile in tensor memory.
@@ -49,8 +50,8 @@ cudaError_t launch_prefill(const CUtensorMap* maps, void* C, const LayerShape& s
 // [N][ldq] box {32,128} SW128; scales [ng][lds] box {128, gps}; zeros [ng][ldz]
 // box {16, gps}, gps = decode_scale_box_rows(g_eff, ng).
 int tmem_gemm_token_tile(int64_t M);
-cudaError_t launch_tmem_gemm(const CUtensorMap* maps, void* C, const LayerShape& s, int num_sms,
-                             bool prefetch_weights, cudaStream_t stream);
+cudaError_t launch_tmem_gemm(const CUtensorMap* maps, void* C, const void* bias, const LayerShape& s,
+                             int num_sms, bool prefetch_weights, cudaStream_t stream);
 int take_status_tmem_gemm();
 
 // Status words of each module: read-and-clear (synchronous).

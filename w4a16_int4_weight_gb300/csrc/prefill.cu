@@ -45,6 +45,7 @@ __device__ __forceinline__ int* p_status() { return &g_status; }
 
 struct Params {
     uint16_t* C;
+    const uint16_t* bias;   // [N] dtype, added before the final rounding; may be null
     int M, N, K, g_eff, ng;
     int nkb;   // ceil(K / kBK)
 };
@@ -212,6 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             const uint32_t lane_base = uint32_t(32 * (warp & 3)) << 16;
             const int n_out = n0 + 32 * (warp & 3) + lane;
             const bool row_ok = n_out < p.N;
+            const float b = p.bias && row_ok ? to_f32<BF16>(p.bias[n_out]) : 0.f;
 #pragma unroll 1
             for (int c = (warp >> 2) * (BT / 64); c < ((warp >> 2) + 1) * (BT / 64); ++c) {
                 uint32_t r[32];
@@ -222,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const int tok = tok0 + j;
-                        if (tok < p.M) p.C[size_t(tok) * p.N + n_out] = from_f32<BF16>(__uint_as_float(r[j]));
+                        if (tok < p.M) p.C[size_t(tok) * p.N + n_out] = from_f32<BF16>(__uint_as_float(r[j]) + b);
                     }
                 }
             }
@@ -259,10 +261,11 @@ cudaError_t launch_bt(const CUtensorMap* maps, const Params& p, bool bf16, bool 
 
 }  // namespace
 
-cudaError_t launch_prefill(const CUtensorMap* maps, void* C, const LayerShape& s, bool dense,
+cudaError_t launch_prefill(const CUtensorMap* maps, void* C, const void* bias, const LayerShape& s, bool dense,
                            int token_tile, cudaStream_t stream) {
     Params p;
     p.C = static_cast<uint16_t*>(C);
+    p.bias = static_cast<const uint16_t*>(bias);
     p.M = int(s.M);
     p.N = int(s.N);
     p.K = int(s.K);

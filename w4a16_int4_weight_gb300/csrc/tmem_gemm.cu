@@ -129,10 +129,11 @@ int tmem_gemm_ksplit(int64_t M, int64_t N, int64_t K, int num_sms) {
     return ks;
 }
 
-cudaError_t launch_tmem_gemm(const CUtensorMap* maps, void* C, const LayerShape& s, int num_sms,
-                             bool prefetch_weights, cudaStream_t stream) {
+cudaError_t launch_tmem_gemm(const CUtensorMap* maps, void* C, const void* bias, const LayerShape& s,
+                             int num_sms, bool prefetch_weights, cudaStream_t stream) {
     tgemm::Params p;
     p.C = static_cast<uint16_t*>(C);
+    p.bias = static_cast<const uint16_t*>(bias);
     p.status = status_ptr();
     if (!p.status) return cudaErrorSymbolNotFound;
     p.M = int(s.M);

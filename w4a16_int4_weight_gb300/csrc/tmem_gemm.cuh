@@ -59,6 +59,7 @@ constexpr int kWStageBytes = (kPkBytes + kScBytes + kZpBytes + 1023) / 1024 * 10
 
 struct Params {
     uint16_t* C;
+    const uint16_t* bias;   // [N] dtype, added before the final rounding; may be null
     int* status;
     int M, N, K, g_eff, ng;
     int gps;           // group rows per weight stage: min(8, 256 / g_eff), 1 for one group
@@ -437,9 +438,12 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BT)) tmem_gemm_kernel(c
     const bool epi = warp < 4 * kHalves;
     const int row = 32 * (warp & 3) + lane;
     const int c0 = (warp >> 2) * kColsPerWarp;
+    // the bias of an output row, 0 without one
+    auto bias_of = [&](int n) { return p.bias && n < p.N ? to_f32<BF16>(p.bias[n]) : 0.f; };
     if (p.ks == 1) {
         if (epi && ok && nkb > 0) {
             const int n = n0 + row;
+            const float b = bias_of(n);
 #pragma unroll 1
             for (int c = 0; c < kColsPerWarp; c += 16) {
                 uint32_t r[16];
@@ -449,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BT)) tmem_gemm_kernel(c
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int tok = m0 + c0 + c + j;
-                        if (tok < p.M) p.C[size_t(tok) * p.N + n] = from_f32<BF16>(__uint_as_float(r[j]));
+                        if (tok < p.M) p.C[size_t(tok) * p.N + n] = from_f32<BF16>(__uint_as_float(r[j]) + b);
                     }
                 }
             }
@@ -488,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BT)) tmem_gemm_kernel(c
         float sum = 0.f;
         for (int c = 0; c < p.ks; ++c) sum += red[(size_t(c) * rows_per + rl) * BT + col];
         const int n = n0 + rank * rows_per + rl, tok = m0 + col;
-        if (n < p.N && tok < p.M && !any_failed) p.C[size_t(tok) * p.N + n] = from_f32<BF16>(sum);
+        if (n < p.N && tok < p.M && !any_failed) p.C[size_t(tok) * p.N + n] = from_f32<BF16>(sum + bias_of(n));
     }
     tc_fence_before();
     __syncthreads();

@@ -174,7 +174,7 @@ int token_tile_for(int64_t M) {
 }
 
 w4a16_status launch_tcgen05(const void* A, const void* Wsrc, bool dense, const void* scales,
-                            const int32_t* zeros, void* C, const LayerShape& s,
+                            const int32_t* zeros, const void* bias, void* C, const LayerShape& s,
                             cudaStream_t stream) {
     const int bt = token_tile_for(s.M);
     CUtensorMap maps[4];
@@ -203,13 +203,13 @@ w4a16_status launch_tcgen05(const void* A, const void* Wsrc, bool dense, const v
             maps[3] = maps[2];   // unused without zero points
         }
     }
-    cudaError_t e = launch_prefill(maps, C, s, dense, bt, stream);
+    cudaError_t e = launch_prefill(maps, C, bias, s, dense, bt, stream);
     if (e != cudaSuccess) return cuda_fail(e, "tcgen05 GEMM launch");
     return W4A16_OK;
 }
 
 w4a16_status launch_tmem_path(const void* A, const void* Wq, const void* scales,
-                              const int32_t* zeros, void* C, const LayerShape& s,
+                              const int32_t* zeros, const void* bias, void* C, const LayerShape& s,
                               bool static_weights, cudaStream_t stream) {
     int sms = 0;
     w4a16_status st = device_sms(&sms);
@@ -234,13 +234,13 @@ w4a16_status launch_tmem_path(const void* A, const void* Wq, const void* scales,
     } else {
         maps[3] = maps[2];   // unused without zero points
     }
-    cudaError_t e = launch_tmem_gemm(maps, C, s, sms, static_weights, stream);
+    cudaError_t e = launch_tmem_gemm(maps, C, bias, s, sms, static_weights, stream);
     if (e != cudaSuccess) return cuda_fail(e, "tensor-memory GEMM launch");
     return W4A16_OK;
 }
 
 w4a16_status launch_decode_path(const void* A, const void* Wq, const void* scales,
-                                const int32_t* zeros, void* C, const LayerShape& s,
+                                const int32_t* zeros, const void* bias, void* C, const LayerShape& s,
                                 bool static_weights, cudaStream_t stream) {
     int sms = 0;
     w4a16_status st = device_sms(&sms);
@@ -263,7 +263,7 @@ w4a16_status launch_decode_path(const void* A, const void* Wq, const void* scale
     } else {
         maps[3] = maps[2];   // unused without zero points
     }
-    cudaError_t e = launch_decode(maps, C, s, sms, static_weights, stream);
+    cudaError_t e = launch_decode(maps, C, bias, s, sms, static_weights, stream);
     if (e != cudaSuccess) return cuda_fail(e, "decode GEMM launch");
     return W4A16_OK;
 }
@@ -326,10 +326,10 @@ int w4a16_route(int64_t M, int64_t N, int64_t K, int G, int qtype, int dtype, in
     return route_impl(s, has_dense != 0);
 }
 
-w4a16_status w4a16_gemm_ex(const void* A, const void* Wq, const void* scales,
-                           const int32_t* zeros, const void* Wdense, void* C, int64_t M,
-                           int64_t N, int64_t K, int G, int qtype, int dtype, int path,
-                           void* stream) {
+w4a16_status w4a16_linear(const void* A, const void* Wq, const void* scales,
+                          const int32_t* zeros, const void* bias, const void* Wdense, void* C,
+                          int64_t M, int64_t N, int64_t K, int G, int qtype, int dtype, int path,
+                          void* stream) {
     LayerShape s;
     w4a16_status st = check_weight(N, K, G, qtype, dtype, &s);
     if (st) return st;
@@ -343,6 +343,7 @@ w4a16_status w4a16_gemm_ex(const void* A, const void* Wq, const void* scales,
     if (!A || !aligned(A, 16)) return fail(W4A16_ERR_INVALID_ARG, "A must be a non-null 16-byte aligned device pointer");
     if (!C || !aligned(C, 2)) return fail(W4A16_ERR_INVALID_ARG, "C must be a non-null 2-byte aligned device pointer");
     if (Wdense && !aligned(Wdense, 16)) return fail(W4A16_ERR_INVALID_ARG, "Wdense must be 16-byte aligned");
+    if (bias && !aligned(bias, 2)) return fail(W4A16_ERR_INVALID_ARG, "bias must be 2-byte aligned");
     s.M = M;
     if (path == W4A16_PATH_AUTO) path = route_impl(s, Wdense != nullptr);
     if (path == W4A16_PATH_FUSED) path = fused_kernel_for(M);
@@ -357,11 +358,20 @@ w4a16_status w4a16_gemm_ex(const void* A, const void* Wq, const void* scales,
     g_err[0] = '\0';
     if (M == 0) return W4A16_OK;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const bool static_weights = (opts & W4A16_OPT_STATIC_WEIGHTS) != 0;
     if (path == W4A16_PATH_DECODE)
-        return launch_decode_path(A, Wq, scales, zeros, C, s, (opts & W4A16_OPT_STATIC_WEIGHTS) != 0, cs);
-    if (path == W4A16_PATH_DENSE) return launch_tcgen05(A, Wdense, true, nullptr, nullptr, C, s, cs);
-    if (path == W4A16_PATH_FUSED_SMEM) return launch_tcgen05(A, Wq, false, scales, zeros, C, s, cs);
-    return launch_tmem_path(A, Wq, scales, zeros, C, s, (opts & W4A16_OPT_STATIC_WEIGHTS) != 0, cs);
+        return launch_decode_path(A, Wq, scales, zeros, bias, C, s, static_weights, cs);
+    if (path == W4A16_PATH_DENSE) return launch_tcgen05(A, Wdense, true, nullptr, nullptr, bias, C, s, cs);
+    if (path == W4A16_PATH_FUSED_SMEM) return launch_tcgen05(A, Wq, false, scales, zeros, bias, C, s, cs);
+    return launch_tmem_path(A, Wq, scales, zeros, bias, C, s, static_weights, cs);
+}
+
+w4a16_status w4a16_gemm_ex(const void* A, const void* Wq, const void* scales,
+                           const int32_t* zeros, const void* Wdense, void* C, int64_t M,
+                           int64_t N, int64_t K, int G, int qtype, int dtype, int path,
+                           void* stream) {
+    return w4a16_linear(A, Wq, scales, zeros, nullptr, Wdense, C, M, N, K, G, qtype, dtype, path,
+                        stream);
 }
 
 w4a16_status w4a16_gemm(const void* A, const void* Wq, const void* scales, const int32_t* zeros,
@@ -409,7 +419,7 @@ w4a16_status w4a16_gemm_dense(const void* A, const void* W, void* C, int64_t M, 
     s.ldz = (N / 8 + 3) / 4 * 4;
     s.bf16 = dtype == W4A16_BF16;
     s.zp = false;
-    return launch_tcgen05(A, W, true, nullptr, nullptr, C, s, static_cast<cudaStream_t>(stream));
+    return launch_tcgen05(A, W, true, nullptr, nullptr, nullptr, C, s, static_cast<cudaStream_t>(stream));
 }
 
 w4a16_status w4a16_device_status(int* site) {
