@@ -71,6 +71,11 @@ def _load():
             "orc_gemm_pairs": (None, [P, P, P, P, I64, I64, I, P]),
             "orc_linear_rows": (I, [P, P, I64, P, P, P, I64, I64, I64, I64, I, P]),
             "orc_add_bias": (None, [P, I64, I64, P, I]),
+            "orc_encode_gptq": (None, [P, I64, I64, P]),
+            "orc_decode_gptq": (None, [P, I64, I64, P]),
+            "orc_encode_kn": (None, [P, I64, I64, P]),
+            "orc_decode_kn": (None, [P, I64, I64, P]),
+            "orc_encode_exllama": (None, [P, I64, I64, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -135,6 +140,30 @@ def unpack_q(words: np.ndarray, K: int) -> np.ndarray:
     N, ldq = w.shape
     out = np.empty((N, K), dtype=np.uint8)
     _load().orc_unpack_q(_ptr(w), N, K, ldq, _ptr(out))
+    return out
+
+
+def encode_q(q, fmt: str) -> np.ndarray:
+    """Unpacked q [N, K] -> checkpoint words: "gptq" [N, K/8] (sequential along K),
+    "exllama" [N, K/8] (shuffled), "kn" [K, N/8] (sequential along N)."""
+    qq = _c(q, np.uint8)
+    N, K = qq.shape
+    lib = _load()
+    if fmt == "kn":
+        out = np.empty((K, N // 8), dtype=np.uint32)
+        lib.orc_encode_kn(_ptr(qq), N, K, _ptr(out))
+    else:
+        out = np.empty((N, K // 8), dtype=np.uint32)
+        {"gptq": lib.orc_encode_gptq, "exllama": lib.orc_encode_exllama}[fmt](_ptr(qq), N, K, _ptr(out))
+    return out
+
+
+def decode_q(words, fmt: str, N: int, K: int) -> np.ndarray:
+    """Checkpoint words ("gptq" or "kn") -> unpacked q [N, K]."""
+    w = _c(words, np.uint32)
+    out = np.empty((N, K), dtype=np.uint8)
+    lib = _load()
+    {"gptq": lib.orc_decode_gptq, "kn": lib.orc_decode_kn}[fmt](_ptr(w), N, K, _ptr(out))
     return out
 
 

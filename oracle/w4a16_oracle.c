@@ -189,6 +189,50 @@ void orc_dequant(const uint8_t* q, const uint16_t* scales, const int32_t* zeros,
 }
 
 /* ------------------------------------------------------------------------- */
+/* Checkpoint word formats the pages read (all 4-bit values, 8 per int32):      */
+/*  - GPTQ / compressed-tensors ("triton_w4a16" page, repack_w_q): [N][K/8],   */
+/*    K-value 8j+i of row n at bits 4i of word j (sequential shifts 0..28).    */
+/*  - the MI300 kernel's layout (same function, step 4): [K][N/8], N-value      */
+/*    8j+i of row k at bits 4i of word j.                                      */
+/*  - the ExLlama shuffle ("rdna_hybrid_w4a16", pack_int4_exllama_shuffle):   */
+/*    [N][K/8], K-value 8j+i at value_shift(i) (orc_pack_q without padding).   */
+/* Encoders from unpacked q [N][K] and decoders back to it.                     */
+/* ------------------------------------------------------------------------- */
+void orc_encode_gptq(const uint8_t* q, int64_t N, int64_t K, uint32_t* out) {
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t j = 0; j < K / 8; ++j) {
+            uint32_t w = 0;
+            for (int i = 0; i < 8; ++i) w |= (uint32_t)(q[n * K + 8 * j + i] & 0xF) << (4 * i);
+            out[n * (K / 8) + j] = w;
+        }
+}
+
+void orc_decode_gptq(const uint32_t* src, int64_t N, int64_t K, uint8_t* q) {
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k)
+            q[n * K + k] = (uint8_t)((src[n * (K / 8) + k / 8] >> (4 * (k % 8))) & 0xF);
+}
+
+void orc_encode_kn(const uint8_t* q, int64_t N, int64_t K, uint32_t* out) {
+    for (int64_t k = 0; k < K; ++k)
+        for (int64_t j = 0; j < N / 8; ++j) {
+            uint32_t w = 0;
+            for (int i = 0; i < 8; ++i) w |= (uint32_t)(q[(8 * j + i) * K + k] & 0xF) << (4 * i);
+            out[k * (N / 8) + j] = w;
+        }
+}
+
+void orc_decode_kn(const uint32_t* src, int64_t N, int64_t K, uint8_t* q) {
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k)
+            q[n * K + k] = (uint8_t)((src[k * (N / 8) + n / 8] >> (4 * (n % 8))) & 0xF);
+}
+
+void orc_encode_exllama(const uint8_t* q, int64_t N, int64_t K, uint32_t* out) {
+    orc_pack_q(q, N, K, K / 8, out);
+}
+
+/* ------------------------------------------------------------------------- */
 /* GEMM in float64:  C[m][n] = sum_k A[m][k] * W[n][k]                          */
 /* ------------------------------------------------------------------------- */
 

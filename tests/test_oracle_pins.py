@@ -406,3 +406,36 @@ def test_bias_is_added_per_output_feature():
     C0 = orc.linear(x.A, x.q, x.scales, None, 64, "bf16")
     C1 = orc.linear(x.A, x.q, x.scales, None, 64, "bf16", bias=bias)
     assert np.allclose(C1 - C0, np.broadcast_to(orc.values(bias, "bf16"), C0.shape), rtol=0, atol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# Checkpoint word formats (GPTQ sequential, the MI300 [K, N/8] layout, ExLlama)
+# --------------------------------------------------------------------------
+
+def test_gptq_word_of_values_0_to_7_is_sequential():
+    # the pages unpack GPTQ words with shifts 0, 4, ..., 28: values 0..7 -> 0x76543210
+    q = np.arange(8, dtype=np.uint8)[None, :]
+    assert orc.encode_q(q, "gptq")[0, 0] == 0x76543210
+    assert orc.encode_q(q, "exllama")[0, 0] == 0x75316420
+
+
+def test_kn_word_packs_eight_output_rows():
+    # [K, N/8]: word (k, j) holds rows 8j..8j+7 of column k at bits 4i
+    q = np.zeros((16, 8), dtype=np.uint8)
+    q[8:16, 3] = np.arange(8)          # rows 8..15, K-value 3
+    w = orc.encode_q(q, "kn")
+    assert w.shape == (8, 2)
+    assert w[3, 1] == 0x76543210 and w[3, 0] == 0 and np.count_nonzero(w) == 1
+
+
+@pytest.mark.parametrize("fmt", ["gptq", "kn"])
+def test_checkpoint_formats_round_trip(fmt):
+    rng = np.random.default_rng(21)
+    q = rng.integers(0, 16, (24, 48)).astype(np.uint8)
+    assert np.array_equal(orc.decode_q(orc.encode_q(q, fmt), fmt, 24, 48), q)
+
+
+def test_exllama_words_match_the_packed_section_without_padding():
+    rng = np.random.default_rng(22)
+    q = rng.integers(0, 16, (5, 40)).astype(np.uint8)    # K/8 = 5, ldq = 8
+    assert np.array_equal(orc.encode_q(q, "exllama"), orc.pack_q(q, 8)[:, :5])
