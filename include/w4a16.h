@@ -100,6 +100,25 @@ w4a16_status w4a16_packed_layout(int64_t N, int64_t K, int G, int qtype, int dty
                                  int64_t* ldq_words);
 
 /*
+ * Source layouts w4a16_pack_ex reads (checkpoint formats on the pages).
+ */
+typedef enum {
+    W4A16_Q_UNPACKED = 0,   /* uint8 [N][K], one value per byte (w4a16_pack's input) */
+    W4A16_Q_GPTQ = 1,       /* int32 [N][K/8]: K-value 8j+i of row n at bits 4i of word j
+                               (GPTQ / compressed-tensors; triton_w4a16 page, repack_w_q) */
+    W4A16_Q_EXLLAMA = 2,    /* int32 [N][K/8]: K-value 8j+i at bits 4*(i/2) + 16*(i%2)
+                               (rdna_hybrid_w4a16, pack_int4_exllama_shuffle) */
+    W4A16_Q_KN = 3          /* int32 [K][N/8]: N-value 8j+i of K-row k at bits 4i of word j
+                               (the MI300 kernel's layout, repack_w_q step 4); N % 8 == 0 */
+} w4a16_qformat;
+
+typedef enum {
+    W4A16_LAYOUT_NG = 0,    /* scales [N][K/G_eff], zeros [N/8][K/G_eff] (compressed-tensors) */
+    W4A16_LAYOUT_GN = 1     /* scales [K/G_eff][N], zeros [K/G_eff][N/8] (AutoGPTQ; the MI300
+                               kernel's repacked form) */
+} w4a16_param_layout;
+
+/*
  * w4a16_pack - relayout one quantised weight into the packed buffer.
  * (Prior art: process_weights_after_loading -> pack_skinny_int4 /
  *  pack_int4_exllama_shuffle on the rdna_hybrid_w4a16 pages; repack_w_q on
@@ -112,6 +131,21 @@ w4a16_status w4a16_packed_layout(int64_t N, int64_t K, int G, int qtype, int dty
  *            must not overlap the inputs.  Fully overwritten, padding included.
  * Enqueues one or two kernels on `stream`.
  */
+/*
+ * w4a16_pack_ex - w4a16_pack from a checkpoint's own word format: the packed
+ * buffer it writes is the one w4a16_pack writes from the same values (bit for
+ * bit, padding included), without an unpacked [N][K] copy in between.
+ *   qsrc          device words in `qformat` (w4a16_qformat); 4-byte aligned
+ *                 (8-byte for W4A16_Q_UNPACKED).
+ *   param_layout  w4a16_param_layout of scales and zeros.
+ *   Other arguments as for w4a16_pack.  W4A16_ERR_INVALID_ARG for an unknown
+ *   format or layout, or W4A16_Q_KN with N % 8 != 0.  Enqueues two or three
+ *   kernels on `stream`.
+ */
+w4a16_status w4a16_pack_ex(const void* qsrc, int qformat, const void* scales, const int32_t* zeros,
+                           int param_layout, void* Wpacked, int64_t N, int64_t K, int G, int qtype,
+                           int dtype, void* stream);
+
 w4a16_status w4a16_pack(const uint8_t* q, const void* scales, const int32_t* zeros,
                         void* Wpacked, int64_t N, int64_t K, int G, int qtype, int dtype,
                         void* stream);

@@ -131,3 +131,14 @@ def test_linear_rejects_a_misaligned_bias(B):
     code = B.lib.w4a16_linear(FAKE, FAKE, FAKE, None, FAKE + 1, None, FAKE, 4, 256, 4096, 128, 0, 1, 0, None)
     assert code == B.ERR_INVALID_ARG
     assert "bias" in B.last_error()
+
+
+def test_pack_ex_rejects_bad_formats(B):
+    assert B.lib.w4a16_pack_ex(FAKE, 7, FAKE, None, 0, FAKE + 256, 64, 64, 32, 0, 0, None) == B.ERR_INVALID_ARG
+    assert "format" in B.last_error()
+    assert B.lib.w4a16_pack_ex(FAKE, 1, FAKE, None, 5, FAKE + 256, 64, 64, 32, 0, 0, None) == B.ERR_INVALID_ARG
+    assert "layout" in B.last_error()
+    assert B.lib.w4a16_pack_ex(FAKE, 3, FAKE, None, 0, FAKE + 256, 60, 64, 32, 0, 0, None) == B.ERR_INVALID_ARG
+    assert "N divisible by 8" in B.last_error()
+    assert B.lib.w4a16_pack_ex(FAKE + 2, 1, FAKE, None, 0, FAKE + 256, 64, 64, 32, 0, 0, None) == B.ERR_INVALID_ARG
+    assert "4-byte aligned" in B.last_error()

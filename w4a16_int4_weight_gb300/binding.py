@@ -48,6 +48,7 @@ _SIGS = {
     "w4a16_last_error_string": (ctypes.c_char_p, []),
     "w4a16_packed_layout": (_I, [_I64, _I64, _I, _I, _I, _SZ, _SZ, _SZ, ctypes.POINTER(_I64)]),
     "w4a16_pack": (_I, [_P, _P, _P, _P, _I64, _I64, _I, _I, _I, _P]),
+    "w4a16_pack_ex": (_I, [_P, _I, _P, _P, _I, _P, _I64, _I64, _I, _I, _I, _P]),
     "w4a16_gemm": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _P]),
     "w4a16_gemm_ex": (_I, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _I, _P]),
     "w4a16_linear": (_I, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _I, _P]),
@@ -149,6 +150,19 @@ def linear(A, Wq, scales, zeros, bias, Wdense, C, M, N, K, G, qtype, dtype, path
         p |= OPT_STATIC_WEIGHTS
     _check(lib.w4a16_linear(_ptr(A), _ptr(Wq), _ptr(scales), _ptr(zeros), _ptr(bias), _ptr(Wdense),
                             _ptr(C), M, N, K, G, _qt(qtype), _dt(dtype), p, _stream(stream)))
+
+
+QFORMATS = {"unpacked": 0, "gptq": 1, "exllama": 2, "kn": 3}
+LAYOUTS = {"ng": 0, "gn": 1}
+
+
+def pack_ex(qsrc, qformat, scales, zeros, param_layout, Wpacked, N, K, G, qtype, dtype, stream=None):
+    """Pack from a checkpoint word format ("unpacked", "gptq", "exllama", "kn"), scales and
+    zeros laid out "ng" ([N][ng], [N/8][ng]) or "gn" ([ng][N], [ng][N/8])."""
+    f = QFORMATS[qformat] if isinstance(qformat, str) else int(qformat)
+    lay = LAYOUTS[param_layout] if isinstance(param_layout, str) else int(param_layout)
+    _check(lib.w4a16_pack_ex(_ptr(qsrc), f, _ptr(scales), _ptr(zeros), lay, _ptr(Wpacked), N, K, G,
+                             _qt(qtype), _dt(dtype), _stream(stream)))
 
 
 def route(M, N, K, G, qtype, dtype, has_dense=False) -> int:

@@ -19,10 +19,12 @@ struct LayerShape {
     bool zp;         // explicit zero points (uint4)
 };
 
-// pack_dequant.cu
-cudaError_t launch_pack(const uint8_t* q, const void* scales, const int32_t* zeros, void* Wq,
-                        void* scales_dst, void* zeros_dst, const LayerShape& s,
-                        cudaStream_t stream);
+// pack_dequant.cu.  qformat: the w4a16_qformat values; groups_first: scales
+// [ng][N] and zeros [ng][N/8] (else [N][ng] and [N/8][ng]).
+constexpr int kQUnpacked = 0, kQGptq = 1, kQExllama = 2, kQKn = 3;
+cudaError_t launch_pack(const void* qsrc, int qformat, const void* scales, const int32_t* zeros,
+                        bool groups_first, void* Wq, void* scales_dst, void* zeros_dst,
+                        const LayerShape& s, cudaStream_t stream);
 cudaError_t launch_dequant(const uint32_t* Wq, const void* scales, const int32_t* zeros,
                            void* W, const LayerShape& s, cudaStream_t stream);
 

@@ -36,6 +36,75 @@ __global__ void __launch_bounds__(kThreads) pack_q_kernel(const uint8_t* __restr
     }
 }
 
+// ExLlama position of K-value i (0..7) within its word.
+__device__ __forceinline__ int exl_shift(int i) { return 4 * (i >> 1) + 16 * (i & 1); }
+
+// GPTQ / compressed-tensors words [N][K/8] (K-value 8j+i at bits 4i) -> the
+// packed section: the eight nibbles of each word move to their ExLlama places.
+__global__ void __launch_bounds__(kThreads) repack_gptq_kernel(const uint32_t* __restrict__ src,
+                                                               uint32_t* __restrict__ out, int N,
+                                                               int K, int ldq) {
+    const int k8 = K / 8;
+    for (int n = blockIdx.x; n < N; n += gridDim.x) {
+        const uint32_t* srow = src + int64_t(n) * k8;
+        uint32_t* orow = out + int64_t(n) * ldq;
+        for (int j = threadIdx.x; j < ldq; j += kThreads) {
+            uint32_t w = 0;
+            if (j < k8) {
+                const uint32_t v = __ldg(srow + j);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) w |= ((v >> (4 * i)) & 0xFu) << exl_shift(i);
+            }
+            orow[j] = w;
+        }
+    }
+}
+
+// ExLlama words [N][K/8] -> the packed section: the same words, row pitch ldq.
+__global__ void __launch_bounds__(kThreads) repack_exllama_kernel(const uint32_t* __restrict__ src,
+                                                                  uint32_t* __restrict__ out, int N,
+                                                                  int K, int ldq) {
+    const int k8 = K / 8;
+    for (int n = blockIdx.x; n < N; n += gridDim.x)
+        for (int j = threadIdx.x; j < ldq; j += kThreads)
+            out[int64_t(n) * ldq + j] = j < k8 ? __ldg(src + int64_t(n) * k8 + j) : 0u;
+}
+
+// The MI300 layout [K][N/8] (N-value 8c+i of row k at bits 4i) -> the packed
+// section.  Item (j, c): the eight source words of K-values 8j..8j+7 at column
+// c give output word j of rows 8c..8c+7.  Consecutive threads take consecutive
+// columns, so the source reads are coalesced.
+__global__ void __launch_bounds__(kThreads) repack_kn_kernel(const uint32_t* __restrict__ src,
+                                                             uint32_t* __restrict__ out, int N, int K,
+                                                             int ldq) {
+    const int n8 = N / 8, k8 = K / 8;
+    const int64_t items = int64_t(ldq) * n8;
+    for (int64_t it = int64_t(blockIdx.x) * kThreads + threadIdx.x; it < items;
+         it += int64_t(gridDim.x) * kThreads) {
+        const int j = int(it / n8), c = int(it % n8);
+        uint32_t v[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) v[t] = j < k8 ? __ldg(src + int64_t(8 * j + t) * n8 + c) : 0u;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            uint32_t w = 0;
+#pragma unroll
+            for (int t = 0; t < 8; ++t) w |= ((v[t] >> (4 * i)) & 0xFu) << exl_shift(t);
+            out[int64_t(8 * c + i) * ldq + j] = w;
+        }
+    }
+}
+
+// [rows][cols] (row-major) -> [rows][ld] with zero padding for c >= cols.
+template <typename T>
+__global__ void __launch_bounds__(kThreads) copy_pad_kernel(const T* __restrict__ src,
+                                                            T* __restrict__ dst, int64_t rows,
+                                                            int64_t cols, int64_t ld) {
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x)
+        for (int64_t c = threadIdx.x; c < ld; c += kThreads)
+            dst[r * ld + c] = c < cols ? src[r * cols + c] : T(0);
+}
+
 // [rows][cols] (row-major) -> [cols][ld] with zero padding for r >= rows.  The
 // output is written in full and in order (coalesced); the strided reads touch
 // each input element once.  Scales and zero points are a small fraction of the
@@ -108,19 +177,41 @@ int group_shift(const LayerShape& s) {
 
 }  // namespace
 
-cudaError_t launch_pack(const uint8_t* q, const void* scales, const int32_t* zeros, void* Wq,
-                        void* scales_dst, void* zeros_dst, const LayerShape& s,
-                        cudaStream_t stream) {
-    pack_q_kernel<<<grid_for(s.N), kThreads, 0, stream>>>(q, static_cast<uint32_t*>(Wq), int(s.N),
-                                                           int(s.K), int(s.ldq));
+cudaError_t launch_pack(const void* qsrc, int qformat, const void* scales, const int32_t* zeros,
+                        bool groups_first, void* Wq, void* scales_dst, void* zeros_dst,
+                        const LayerShape& s, cudaStream_t stream) {
+    auto* out = static_cast<uint32_t*>(Wq);
+    const int N = int(s.N), K = int(s.K), ldq = int(s.ldq);
+    switch (qformat) {
+        case kQUnpacked:
+            pack_q_kernel<<<grid_for(s.N), kThreads, 0, stream>>>(static_cast<const uint8_t*>(qsrc), out, N, K, ldq);
+            break;
+        case kQGptq:
+            repack_gptq_kernel<<<grid_for(s.N), kThreads, 0, stream>>>(static_cast<const uint32_t*>(qsrc), out, N, K, ldq);
+            break;
+        case kQExllama:
+            repack_exllama_kernel<<<grid_for(s.N), kThreads, 0, stream>>>(static_cast<const uint32_t*>(qsrc), out, N, K, ldq);
+            break;
+        default: {
+            const int64_t items = s.ldq * (s.N / 8);
+            int64_t blocks = (items + kThreads - 1) / kThreads;
+            if (blocks > 152 * 32) blocks = 152 * 32;
+            repack_kn_kernel<<<int(blocks < 1 ? 1 : blocks), kThreads, 0, stream>>>(static_cast<const uint32_t*>(qsrc), out, N, K, ldq);
+        }
+    }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    transpose_pad_kernel<uint16_t><<<grid_for(s.ng), kThreads, 0, stream>>>(
-        static_cast<const uint16_t*>(scales), static_cast<uint16_t*>(scales_dst), s.N, s.ng, s.lds);
+    // scales -> [ng][lds], zero points -> [ng][ldz]: transposed from the
+    // [N][ng] / [N/8][ng] layout, copied from [ng][N] / [ng][N/8]
+    const auto* sc = static_cast<const uint16_t*>(scales);
+    auto* scd = static_cast<uint16_t*>(scales_dst);
+    if (groups_first) copy_pad_kernel<uint16_t><<<grid_for(s.ng), kThreads, 0, stream>>>(sc, scd, s.ng, s.N, s.lds);
+    else transpose_pad_kernel<uint16_t><<<grid_for(s.ng), kThreads, 0, stream>>>(sc, scd, s.N, s.ng, s.lds);
     e = cudaGetLastError();
     if (e != cudaSuccess || !s.zp) return e;
-    transpose_pad_kernel<int32_t><<<grid_for(s.ng), kThreads, 0, stream>>>(
-        zeros, static_cast<int32_t*>(zeros_dst), s.N / 8, s.ng, s.ldz);
+    auto* zd = static_cast<int32_t*>(zeros_dst);
+    if (groups_first) copy_pad_kernel<int32_t><<<grid_for(s.ng), kThreads, 0, stream>>>(zeros, zd, s.ng, s.N / 8, s.ldz);
+    else transpose_pad_kernel<int32_t><<<grid_for(s.ng), kThreads, 0, stream>>>(zeros, zd, s.N / 8, s.ng, s.ldz);
     return cudaGetLastError();
 }
 

@@ -298,12 +298,21 @@ w4a16_status w4a16_packed_layout(int64_t N, int64_t K, int G, int qtype, int dty
     return W4A16_OK;
 }
 
-w4a16_status w4a16_pack(const uint8_t* q, const void* scales, const int32_t* zeros, void* Wpacked,
-                        int64_t N, int64_t K, int G, int qtype, int dtype, void* stream) {
+w4a16_status w4a16_pack_ex(const void* qsrc, int qformat, const void* scales, const int32_t* zeros,
+                           int param_layout, void* Wpacked, int64_t N, int64_t K, int G, int qtype,
+                           int dtype, void* stream) {
     LayerShape s;
     w4a16_status st = check_weight(N, K, G, qtype, dtype, &s);
     if (st) return st;
-    if (!q || !aligned(q, 8)) return fail(W4A16_ERR_INVALID_ARG, "q must be a non-null 8-byte aligned device pointer");
+    if (qformat < W4A16_Q_UNPACKED || qformat > W4A16_Q_KN)
+        return fail(W4A16_ERR_INVALID_ARG, "unknown weight format %d", qformat);
+    if (param_layout != W4A16_LAYOUT_NG && param_layout != W4A16_LAYOUT_GN)
+        return fail(W4A16_ERR_INVALID_ARG, "unknown scale/zero layout %d", param_layout);
+    if (qformat == W4A16_Q_KN && N % 8)
+        return fail(W4A16_ERR_INVALID_ARG, "the [K][N/8] format needs N divisible by 8, got N=%lld", (long long)N);
+    const size_t qalign = qformat == W4A16_Q_UNPACKED ? 8 : 4;
+    if (!qsrc || !aligned(qsrc, qalign))
+        return fail(W4A16_ERR_INVALID_ARG, "q must be a non-null %zu-byte aligned device pointer", qalign);
     if (!Wpacked || !aligned(Wpacked, 256)) return fail(W4A16_ERR_INVALID_ARG, "Wpacked must be a non-null 256-byte aligned device pointer");
     if (!scales || !aligned(scales, 2)) return fail(W4A16_ERR_INVALID_ARG, "scales must be a non-null 2-byte aligned device pointer");
     if (s.zp && (!zeros || !aligned(zeros, 4))) return fail(W4A16_ERR_INVALID_ARG, "uint4 needs a non-null 4-byte aligned zeros pointer");
@@ -311,11 +320,17 @@ w4a16_status w4a16_pack(const uint8_t* q, const void* scales, const int32_t* zer
     size_t total, so, zo;
     w4a16_packed_layout(N, K, G, qtype, dtype, &total, &so, &zo, nullptr);
     uint8_t* base = static_cast<uint8_t*>(Wpacked);
-    cudaError_t e = launch_pack(q, scales, zeros, base, base + so, s.zp ? base + zo : nullptr, s,
-                                static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_pack(qsrc, qformat, scales, zeros, param_layout == W4A16_LAYOUT_GN, base,
+                                base + so, s.zp ? base + zo : nullptr, s, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "pack launch");
     g_err[0] = '\0';
     return W4A16_OK;
+}
+
+w4a16_status w4a16_pack(const uint8_t* q, const void* scales, const int32_t* zeros, void* Wpacked,
+                        int64_t N, int64_t K, int G, int qtype, int dtype, void* stream) {
+    return w4a16_pack_ex(q, W4A16_Q_UNPACKED, scales, zeros, W4A16_LAYOUT_NG, Wpacked, N, K, G,
+                         qtype, dtype, stream);
 }
 
 int w4a16_route(int64_t M, int64_t N, int64_t K, int G, int qtype, int dtype, int has_dense) {
