@@ -206,13 +206,17 @@ w4a16_status w4a16_gemm_ex(const void* A, const void* Wq, const void* scales,
  * output is rounded once (the pages' fused path adds it after rounding, in
  * the dtype: two roundings; both lie within the GEMM tolerance).
  *   bias     device dtype [N], 2-byte aligned, or NULL for none.
+ *   lda      row pitch of A in elements: 0 (= K) or >= K and a multiple of 8
+ *            (16-byte rows, as every kernel reads A by TMA); rows may be padded
+ *            (the pages' stride_am).  The padding is never read.
+ *   ldc      row pitch of C in elements: 0 (= N) or >= N.  Only [M][N] is written.
  *   Every other argument, the validation and the error behaviour are those of
- *   w4a16_gemm_ex, which is w4a16_linear with bias NULL.
+ *   w4a16_gemm_ex, which is w4a16_linear with bias NULL and lda = ldc = 0.
  */
-w4a16_status w4a16_linear(const void* A, const void* Wq, const void* scales,
+w4a16_status w4a16_linear(const void* A, int64_t lda, const void* Wq, const void* scales,
                           const int32_t* zeros, const void* bias, const void* Wdense, void* C,
-                          int64_t M, int64_t N, int64_t K, int G, int qtype, int dtype, int path,
-                          void* stream);
+                          int64_t ldc, int64_t M, int64_t N, int64_t K, int G, int qtype, int dtype,
+                          int path, void* stream);
 
 /*
  * w4a16_route - the kernel w4a16_gemm_ex(..., W4A16_PATH_AUTO, ...) runs for

@@ -127,10 +127,21 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
         spec.loader.exec_module(mod)
 
 
-def test_linear_rejects_a_misaligned_bias(B):
-    code = B.lib.w4a16_linear(FAKE, FAKE, FAKE, None, FAKE + 1, None, FAKE, 4, 256, 4096, 128, 0, 1, 0, None)
+@pytest.mark.parametrize("args,needle", [
+    (dict(bias=FAKE + 1), "bias"),
+    (dict(lda=4000), "lda=4000"),      # < K
+    (dict(lda=4100), "lda=4100"),      # not a multiple of 8
+    (dict(ldc=255), "ldc=255"),        # < N
+])
+def test_linear_rejects_bad_bias_and_strides(B, args, needle):
+    a = dict(A=FAKE, lda=0, Wq=FAKE, scales=FAKE, zeros=None, bias=None, Wdense=None, C=FAKE, ldc=0,
+             M=4, N=256, K=4096, G=128, qtype=0, dtype=1, path=0)
+    a.update(args)
+    code = B.lib.w4a16_linear(a["A"], a["lda"], a["Wq"], a["scales"], a["zeros"], a["bias"], a["Wdense"],
+                              a["C"], a["ldc"], a["M"], a["N"], a["K"], a["G"], a["qtype"], a["dtype"],
+                              a["path"], None)
     assert code == B.ERR_INVALID_ARG
-    assert "bias" in B.last_error()
+    assert needle in B.last_error()
 
 
 def test_pack_ex_rejects_bad_formats(B):

@@ -51,7 +51,7 @@ _SIGS = {
     "w4a16_pack_ex": (_I, [_P, _I, _P, _P, _I, _P, _I64, _I64, _I, _I, _I, _P]),
     "w4a16_gemm": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _P]),
     "w4a16_gemm_ex": (_I, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _I, _P]),
-    "w4a16_linear": (_I, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _I, _P]),
+    "w4a16_linear": (_I, [_P, _I64, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I, _I, _I, _I, _P]),
     "w4a16_route": (_I, [_I64, _I64, _I64, _I, _I, _I, _I]),
     "w4a16_dequant": (_I, [_P, _P, _P, _P, _I64, _I64, _I, _I, _I, _P]),
     "w4a16_gemm_dense": (_I, [_P, _P, _P, _I64, _I64, _I64, _I, _P]),
@@ -143,13 +143,15 @@ def gemm_ex(A, Wq, scales, zeros, Wdense, C, M, N, K, G, qtype, dtype, path="aut
 
 
 def linear(A, Wq, scales, zeros, bias, Wdense, C, M, N, K, G, qtype, dtype, path="auto",
-           stream=None, static_weights=False):
-    """gemm_ex plus bias[N] (dtype) added before the output rounding; bias may be None."""
+           stream=None, static_weights=False, lda=0, ldc=0):
+    """gemm_ex plus bias[N] (dtype) added before the output rounding; bias may be None;
+    lda / ldc: row pitches of A and C in elements (0 = contiguous)."""
     p = PATHS[path] if isinstance(path, str) else int(path)
     if static_weights:
         p |= OPT_STATIC_WEIGHTS
-    _check(lib.w4a16_linear(_ptr(A), _ptr(Wq), _ptr(scales), _ptr(zeros), _ptr(bias), _ptr(Wdense),
-                            _ptr(C), M, N, K, G, _qt(qtype), _dt(dtype), p, _stream(stream)))
+    _check(lib.w4a16_linear(_ptr(A), lda, _ptr(Wq), _ptr(scales), _ptr(zeros), _ptr(bias),
+                            _ptr(Wdense), _ptr(C), ldc, M, N, K, G, _qt(qtype), _dt(dtype), p,
+                            _stream(stream)))
 
 
 QFORMATS = {"unpacked": 0, "gptq": 1, "exllama": 2, "kn": 3}

@@ -53,6 +53,7 @@ constexpr int kMaxGps = 8;               // groups per box at G = 32
 struct Params {
     uint16_t* C;
     const uint16_t* bias;   // [N] dtype, added before the final rounding; may be null
+    int64_t ldc;            // row pitch of C in elements (>= N)
     int* status;      // device status word (first timed-out wait site)
     int M, N, K, g_eff;
     int nboxes;       // ceil(K / kBoxK)
@@ -321,7 +322,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
                     const int tok = 8 * j + 2 * t + (e & 1);
                     const int n = n0 + (e < 2 ? r0 : r1);
                     if (tok < p.M && n < p.N)
-                        p.C[size_t(tok) * p.N + n] = from_f32<BF16>(acc[j][e] + (e < 2 ? b0 : b1));
+                        p.C[size_t(tok) * p.ldc + n] = from_f32<BF16>(acc[j][e] + (e < 2 ? b0 : b1));
                 }
             }
         }
@@ -354,7 +355,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
         float sum = 0.f;
         for (int c = 0; c < p.ks; ++c) sum += red[(c * rows_per + rl) * MP + tok];
         const int n = n0 + rank * rows_per + rl;
-        if (n < p.N && !any_failed) p.C[size_t(tok) * p.N + n] = from_f32<BF16>(sum + bias_of(n));
+        if (n < p.N && !any_failed) p.C[size_t(tok) * p.ldc + n] = from_f32<BF16>(sum + bias_of(n));
     }
 }
 

@@ -17,6 +17,8 @@ struct LayerShape {
     int64_t ldz;     // transposed zero-point row pitch in words: round_up(N/8, 4)
     bool bf16;       // activation dtype
     bool zp;         // explicit zero points (uint4)
+    int64_t lda = 0; // row pitch of A in elements (>= K, a multiple of 8)
+    int64_t ldc = 0; // row pitch of C in elements (>= N)
 };
 
 // pack_dequant.cu.  qformat: the w4a16_qformat values; groups_first: scales

@@ -46,6 +46,7 @@ __device__ __forceinline__ int* p_status() { return &g_status; }
 struct Params {
     uint16_t* C;
     const uint16_t* bias;   // [N] dtype, added before the final rounding; may be null
+    int64_t ldc;            // row pitch of C in elements (>= N)
     int M, N, K, g_eff, ng;
     int nkb;   // ceil(K / kBK)
 };
@@ -224,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const int tok = tok0 + j;
-                        if (tok < p.M) p.C[size_t(tok) * p.N + n_out] = from_f32<BF16>(__uint_as_float(r[j]) + b);
+                        if (tok < p.M) p.C[size_t(tok) * p.ldc + n_out] = from_f32<BF16>(__uint_as_float(r[j]) + b);
                     }
                 }
             }
@@ -266,6 +267,7 @@ cudaError_t launch_prefill(const CUtensorMap* maps, void* C, const void* bias, c
     Params p;
     p.C = static_cast<uint16_t*>(C);
     p.bias = static_cast<const uint16_t*>(bias);
+    p.ldc = s.ldc;
     p.M = int(s.M);
     p.N = int(s.N);
     p.K = int(s.K);

@@ -134,6 +134,7 @@ cudaError_t launch_tmem_gemm(const CUtensorMap* maps, void* C, const void* bias,
     tgemm::Params p;
     p.C = static_cast<uint16_t*>(C);
     p.bias = static_cast<const uint16_t*>(bias);
+    p.ldc = s.ldc;
     p.status = status_ptr();
     if (!p.status) return cudaErrorSymbolNotFound;
     p.M = int(s.M);

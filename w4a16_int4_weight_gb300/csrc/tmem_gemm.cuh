@@ -60,6 +60,7 @@ constexpr int kWStageBytes = (kPkBytes + kScBytes + kZpBytes + 1023) / 1024 * 10
 struct Params {
     uint16_t* C;
     const uint16_t* bias;   // [N] dtype, added before the final rounding; may be null
+    int64_t ldc;            // row pitch of C in elements (>= N)
     int* status;
     int M, N, K, g_eff, ng;
     int gps;           // group rows per weight stage: min(8, 256 / g_eff), 1 for one group
@@ -453,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BT)) tmem_gemm_kernel(c
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int tok = m0 + c0 + c + j;
-                        if (tok < p.M) p.C[size_t(tok) * p.N + n] = from_f32<BF16>(__uint_as_float(r[j]) + b);
+                        if (tok < p.M) p.C[size_t(tok) * p.ldc + n] = from_f32<BF16>(__uint_as_float(r[j]) + b);
                     }
                 }
             }
@@ -492,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BT)) tmem_gemm_kernel(c
         float sum = 0.f;
         for (int c = 0; c < p.ks; ++c) sum += red[(size_t(c) * rows_per + rl) * BT + col];
         const int n = n0 + rank * rows_per + rl, tok = m0 + col;
-        if (n < p.N && tok < p.M && !any_failed) p.C[size_t(tok) * p.N + n] = from_f32<BF16>(sum + bias_of(n));
+        if (n < p.N && tok < p.M && !any_failed) p.C[size_t(tok) * p.ldc + n] = from_f32<BF16>(sum + bias_of(n));
     }
     tc_fence_before();
     __syncthreads();

@@ -68,6 +68,8 @@ w4a16_status check_weight(int64_t N, int64_t K, int G, int qtype, int dtype, Lay
         s->bf16 = dtype == W4A16_BF16;
         s->zp = qtype == W4A16_UINT4;
         s->M = 0;
+        s->lda = K;
+        s->ldc = N;
     }
     return W4A16_OK;
 }
@@ -179,7 +181,7 @@ w4a16_status launch_tcgen05(const void* A, const void* Wsrc, bool dense, const v
     const int bt = token_tile_for(s.M);
     CUtensorMap maps[4];
     w4a16_status st = make_map(&maps[0], A, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, uint64_t(s.K),
-                               uint64_t(s.M), uint64_t(s.K) * 2, 64, uint32_t(bt),
+                               uint64_t(s.M), uint64_t(s.lda) * 2, 64, uint32_t(bt),
                                CU_TENSOR_MAP_SWIZZLE_128B);
     if (st) return st;
     if (dense) {
@@ -219,7 +221,7 @@ w4a16_status launch_tmem_path(const void* A, const void* Wq, const void* scales,
     const uint32_t gps = uint32_t(decode_scale_box_rows(s.g_eff, s.ng));
     CUtensorMap maps[4];
     st = make_map(&maps[0], A, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, uint64_t(s.K), uint64_t(s.M),
-                  uint64_t(s.K) * 2, 64, uint32_t(bt), CU_TENSOR_MAP_SWIZZLE_128B);
+                  uint64_t(s.lda) * 2, 64, uint32_t(bt), CU_TENSOR_MAP_SWIZZLE_128B);
     if (st) return st;
     st = make_map(&maps[1], Wq, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, uint64_t(s.ldq), uint64_t(s.N),
                   uint64_t(s.ldq) * 4, 32, 128, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -251,7 +253,7 @@ w4a16_status launch_decode_path(const void* A, const void* Wq, const void* scale
                   uint64_t(s.ldq) * 4, 32, 128, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st) return st;
     st = make_map(&maps[1], A, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, uint64_t(s.K), uint64_t(s.M),
-                  uint64_t(s.K) * 2, 256, uint32_t(s.M), CU_TENSOR_MAP_SWIZZLE_NONE);
+                  uint64_t(s.lda) * 2, 256, uint32_t(s.M), CU_TENSOR_MAP_SWIZZLE_NONE);
     if (st) return st;
     st = make_map(&maps[2], scales, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, uint64_t(s.lds), uint64_t(s.ng),
                   uint64_t(s.lds) * 2, 128, gps, CU_TENSOR_MAP_SWIZZLE_NONE);
@@ -341,10 +343,10 @@ int w4a16_route(int64_t M, int64_t N, int64_t K, int G, int qtype, int dtype, in
     return route_impl(s, has_dense != 0);
 }
 
-w4a16_status w4a16_linear(const void* A, const void* Wq, const void* scales,
+w4a16_status w4a16_linear(const void* A, int64_t lda, const void* Wq, const void* scales,
                           const int32_t* zeros, const void* bias, const void* Wdense, void* C,
-                          int64_t M, int64_t N, int64_t K, int G, int qtype, int dtype, int path,
-                          void* stream) {
+                          int64_t ldc, int64_t M, int64_t N, int64_t K, int G, int qtype, int dtype,
+                          int path, void* stream) {
     LayerShape s;
     w4a16_status st = check_weight(N, K, G, qtype, dtype, &s);
     if (st) return st;
@@ -359,6 +361,13 @@ w4a16_status w4a16_linear(const void* A, const void* Wq, const void* scales,
     if (!C || !aligned(C, 2)) return fail(W4A16_ERR_INVALID_ARG, "C must be a non-null 2-byte aligned device pointer");
     if (Wdense && !aligned(Wdense, 16)) return fail(W4A16_ERR_INVALID_ARG, "Wdense must be 16-byte aligned");
     if (bias && !aligned(bias, 2)) return fail(W4A16_ERR_INVALID_ARG, "bias must be 2-byte aligned");
+    if (lda == 0) lda = K;
+    if (ldc == 0) ldc = N;
+    if (lda < K || lda > kMaxDim || lda % 8)
+        return fail(W4A16_ERR_INVALID_ARG, "lda=%lld must be >= K=%lld and a multiple of 8 (16-byte row pitch)", (long long)lda, (long long)K);
+    if (ldc < N || ldc > kMaxDim) return fail(W4A16_ERR_INVALID_ARG, "ldc=%lld must be >= N=%lld", (long long)ldc, (long long)N);
+    s.lda = lda;
+    s.ldc = ldc;
     s.M = M;
     if (path == W4A16_PATH_AUTO) path = route_impl(s, Wdense != nullptr);
     if (path == W4A16_PATH_FUSED) path = fused_kernel_for(M);
@@ -385,8 +394,8 @@ w4a16_status w4a16_gemm_ex(const void* A, const void* Wq, const void* scales,
                            const int32_t* zeros, const void* Wdense, void* C, int64_t M,
                            int64_t N, int64_t K, int G, int qtype, int dtype, int path,
                            void* stream) {
-    return w4a16_linear(A, Wq, scales, zeros, nullptr, Wdense, C, M, N, K, G, qtype, dtype, path,
-                        stream);
+    return w4a16_linear(A, 0, Wq, scales, zeros, nullptr, Wdense, C, 0, M, N, K, G, qtype, dtype,
+                        path, stream);
 }
 
 w4a16_status w4a16_gemm(const void* A, const void* Wq, const void* scales, const int32_t* zeros,
@@ -434,6 +443,8 @@ w4a16_status w4a16_gemm_dense(const void* A, const void* W, void* C, int64_t M, 
     s.ldz = (N / 8 + 3) / 4 * 4;
     s.bf16 = dtype == W4A16_BF16;
     s.zp = false;
+    s.lda = K;
+    s.ldc = N;
     return launch_tcgen05(A, W, true, nullptr, nullptr, nullptr, C, s, static_cast<cudaStream_t>(stream));
 }
 
