@@ -32,6 +32,7 @@ SHAPES = [
     (40, 136, 4112, -1, "uint4b8", "bf16"),
     (513, 1024, 2048, 32, "uint4", "bf16"),
     (129, 256, 1024, 256, "uint4", "fp16"),
+    (12, 256, 1024, 32, "uint4", "bf16"),      # G = 32 between 9 and 16 tokens: routed to the fused kernel
 ]
 
 
