@@ -80,18 +80,20 @@ constexpr int tmem_stages_for(int bt) { return bt <= 128 ? 4 : 8; }
 // split-K buffer at BT >= 64), 96-128 KB of packed weights in flight per SM.
 template <int BT>
 struct Layout {
-    // The MMA issuer takes K blocks in units of kUnit: one wait and two commits
-    // per unit.  At N <= 64 every M=128, K=16 MMA costs ~45 cycles whatever N, so
-    // pairing blocks there halves the issuer's fixed cost per block.
-    static constexpr int kUnit = BT <= 64 ? 2 : 1;
-    static constexpr int kWStages = BT <= 32 ? 4 : 3;
-    static constexpr int kAUnits = BT <= 16 ? 4 : BT <= 64 ? 2 : 3;   // activation unit-slots
+    // The MMA issuer takes K blocks in units of kUnit = 2: one wait and two
+    // commits per unit, which halves its fixed cost per block (a wait costs the
+    // single issuing thread 130-220 cycles, a commit ~44; measured faster than
+    // one-block units at every token tile, most at 128 tokens: 66 -> 58 us on
+    // the 70B MLP).  Rings sized for two CTAs per SM up to BT = 128.
+    static constexpr int kUnit = 2;
+    static constexpr int kWStages = BT <= 32 ? 4 : BT <= 64 ? 3 : BT <= 128 ? 2 : 3;
+    static constexpr int kAUnits = BT <= 16 ? 4 : 2;                  // activation unit-slots
     static constexpr int kTmemCols = tmem_cols_for(BT);
     static constexpr int kTmemStages = tmem_stages_for(BT);           // 32-column block stages
     static constexpr int kTUnits = kTmemStages / kUnit;               // tensor-memory unit-slots
     static_assert(BT + 32 * kTmemStages <= kTmemCols, "tensor-memory budget");
     static_assert((kTmemStages & (kTmemStages - 1)) == 0, "power-of-two tensor-memory ring");
-    static_assert(kSubPerW % kUnit == 0 && kTUnits >= 2, "units tile a weight stage");
+    static_assert(kUnit == 2 && kSubPerW % kUnit == 0 && kTUnits >= 2, "two-block units tile a weight stage");
     static constexpr int kActBytes = BT * kBK * 2;                    // one activation tile
     static constexpr int kAUnitBytes = kUnit * kActBytes;
     static constexpr int kActOff = kWStages * kWStageBytes;
@@ -367,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BT)) tmem_gemm_kernel(c
             const uint8_t* stg = pk_tile(s);
             const int b0 = w * kSubPerW;                        // first block of the stage
             const int nj = min(kSubPerW, nkb - b0);
-            if (nj == kSubPerW && kUnit == 2) {
+            if (nj == kSubPerW) {
                 // units (0,1) and (2,3) of the stage
                 const int u0 = b0 / 2;
                 convert(stg, 0, ca);
@@ -388,23 +390,6 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BT)) tmem_gemm_kernel(c
                     put(b0 + 3, cb);
                     ok = unit_done(u0 + 1);
                 }
-            } else if (nj == kSubPerW) {
-                // one block per unit: block j + 1 is converted before block j is handed off
-                auto hand = [&](int li, const uint32_t (&cols)[16]) -> bool {
-                    if (!unit_free(li)) return false;
-                    put(li, cols);
-                    return unit_done(li);
-                };
-                convert(stg, 0, ca);
-                convert(stg, 1, cb);
-                ok = hand(b0, ca);
-                convert(stg, 2, ca);
-                ok = ok && hand(b0 + 1, cb);
-                convert(stg, 3, cb);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&w_empty[s]);
-                ok = ok && hand(b0 + 2, ca);
-                ok = ok && hand(b0 + 3, cb);
             } else {
                 // the last stage of a K range that ends inside it
 #pragma unroll
