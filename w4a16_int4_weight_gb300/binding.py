@@ -83,10 +83,28 @@ def _ptr(x):
     return x.data_ptr()
 
 
+_RAW_STREAM = None
+
+
+def _current_stream_handle():
+    """torch's current CUDA stream on the current device, as a raw handle.  The
+    raw query costs well under a microsecond; torch.cuda.current_stream() builds
+    a Python object per call (several microseconds), which is used only when the
+    raw query is not available."""
+    global _RAW_STREAM
+    import torch
+    if _RAW_STREAM is None:
+        get_dev = getattr(torch._C, "_cuda_getDevice", None)
+        get_raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        _RAW_STREAM = (lambda: get_raw(get_dev())) if get_dev and get_raw else False
+    if _RAW_STREAM:
+        return _RAW_STREAM()
+    return torch.cuda.current_stream().cuda_stream
+
+
 def _stream(stream):
     if stream is None:
-        import torch
-        return torch.cuda.current_stream().cuda_stream
+        return _current_stream_handle()
     if isinstance(stream, int):
         return stream
     return stream.cuda_stream

@@ -363,7 +363,7 @@ template <int NT, bool BF16, bool ZP, int WPG>
 cudaError_t launch_one(const CUtensorMap* maps, const Params& p, int grid, size_t smem,
                        cudaStream_t stream) {
     auto kern = decode_kernel<NT, BF16, ZP, WPG>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    cudaError_t e = ensure_smem(reinterpret_cast<const void*>(kern), int(smem));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);

@@ -6,7 +6,28 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+#include <unordered_map>
+
 namespace w4a16 {
+
+// Dynamic shared memory a kernel may use: cudaFuncSetAttribute once per
+// (kernel, device) and size increase, since the attribute is a per-function
+// maximum that stays set.
+inline cudaError_t ensure_smem(const void* func, int bytes) {
+    static std::mutex mu;
+    static std::unordered_map<uint64_t, int> granted;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t key = uint64_t(reinterpret_cast<uintptr_t>(func)) * 64u + uint64_t(dev & 63);
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = granted.find(key);
+    if (it != granted.end() && it->second >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) granted[key] = bytes;
+    return e;
+}
 
 struct LayerShape {
     int64_t M, N, K;

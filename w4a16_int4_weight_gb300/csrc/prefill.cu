@@ -240,7 +240,7 @@ template <bool BF16, bool ZP, int BT, bool DENSE>
 cudaError_t launch_t(const CUtensorMap* maps, const Params& p, cudaStream_t stream) {
     auto kern = prefill_kernel<BF16, ZP, BT, DENSE>;
     constexpr int smem = Layout<BT, DENSE>::kBytes;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = ensure_smem(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
     const int64_t ctas = int64_t((p.N + kBM - 1) / kBM) * ((p.M + BT - 1) / BT);
     if (ctas > int64_t(0x7fffffff)) return cudaErrorInvalidValue;   // beyond any C that fits in memory

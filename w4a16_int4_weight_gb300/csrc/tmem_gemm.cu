@@ -41,7 +41,7 @@ cudaError_t launch_t(const CUtensorMap* maps, const tgemm::Params& p, int grid_x
     // cluster wait for each other, so more resident CTAs than 512 / kTmemCols
     // could deadlock.  Ask for enough shared memory that no more fit.
     const int smem = tmem_safe_smem(p.ks > 1 ? L::kBytesRed : L::kBytesNoRed, L::kTmemCols);
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = ensure_smem(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid_x, grid_y);

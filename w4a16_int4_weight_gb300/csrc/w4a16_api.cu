@@ -106,9 +106,48 @@ w4a16_status get_encoder() {
 }
 
 // 2-D row-major tensor [rows][cols] of `elem` bytes, box [box_rows][box_cols].
+// Encoded tensor maps, keyed by every input of the encoding (a map is a pure
+// function of them), so that repeated calls on the same buffers - a layer's
+// weight every step, a reused activation buffer - skip the driver encoder.
+struct MapKey {
+    const void* base;
+    uint64_t cols, rows, stride;
+    uint32_t box_cols, box_rows;
+    int dt, swz;
+    bool operator==(const MapKey& o) const {
+        return base == o.base && cols == o.cols && rows == o.rows && stride == o.stride &&
+               box_cols == o.box_cols && box_rows == o.box_rows && dt == o.dt && swz == o.swz;
+    }
+};
+constexpr int kMapCacheSize = 4096;   // direct-mapped
+struct MapEntry {
+    MapKey key;
+    CUtensorMap map;
+    bool valid = false;
+};
+MapEntry g_map_cache[kMapCacheSize];
+std::mutex g_map_mu;
+
+size_t map_slot(const MapKey& k) {
+    uint64_t h = reinterpret_cast<uintptr_t>(k.base) * 0x9E3779B97F4A7C15ull;
+    for (uint64_t v : {k.cols, k.rows, k.stride, uint64_t(k.box_cols) << 32 | k.box_rows,
+                       uint64_t(uint32_t(k.dt)) << 32 | uint32_t(k.swz)})
+        h = (h ^ v) * 0x100000001B3ull;
+    return size_t(h >> 52) % kMapCacheSize;
+}
+
 w4a16_status make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem,
                       uint64_t cols, uint64_t rows, uint64_t row_stride_bytes, uint32_t box_cols,
                       uint32_t box_rows, CUtensorMapSwizzle swz) {
+    const MapKey key{base, cols, rows, row_stride_bytes, box_cols, box_rows, int(dt), int(swz)};
+    const size_t slot = map_slot(key);
+    {
+        std::lock_guard<std::mutex> lk(g_map_mu);
+        if (g_map_cache[slot].valid && g_map_cache[slot].key == key) {
+            *m = g_map_cache[slot].map;
+            return W4A16_OK;
+        }
+    }
     w4a16_status st = get_encoder();
     if (st) return st;
     cuuint64_t dims[2] = {cols, rows};
@@ -122,6 +161,10 @@ w4a16_status make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, 
     if (r != CUDA_SUCCESS)
         return fail(W4A16_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d) for a %llux%llu tensor",
                     int(r), (unsigned long long)rows, (unsigned long long)cols);
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    g_map_cache[slot].key = key;
+    g_map_cache[slot].map = *m;
+    g_map_cache[slot].valid = true;
     return W4A16_OK;
 }
 
