@@ -124,6 +124,16 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     const int nb = b_hi - b_lo;
     const int k_hi = min(p.K, b_hi * kBoxK);
 
+    if (p.M < MP && warp < kConsumerWarps) {
+        // Token rows past M stay zero for the whole kernel: the activation loads
+        // write rows < M only, so the MMA operand loads need no token check.
+        const int row_bytes = kBoxK * 2, pad = (MP - p.M) * row_bytes;
+        for (int s = 0; s < p.stages; ++s) {
+            uint8_t* a = stage_view(smem, p, s).a + p.M * row_bytes;
+            for (int o = tid * 16; o < pad; o += kConsumerWarps * 32 * 16)
+                *reinterpret_cast<uint4*>(a + o) = make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
     if (tid == 0) {
         for (int s = 0; s < kMaxStages; ++s) {
             mbar_init(&full[s], 1);
@@ -172,13 +182,15 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
             // the next kernel in the stream may start its own prologue now
             grid_launch_dependents();
             int issued = first;
+            int s = first % p.stages;                        // ring slot of box `issued`
+            uint32_t wrap = uint32_t(first / p.stages) & 1u;  // its pass over the ring, mod 2
             for (; issued < nb; ++issued) {
-                const int s = issued % p.stages;
-                if (!mbar_wait(&empty[s], uint32_t(issued / p.stages - 1) & 1u, p.status, 3)) break;
+                if (!mbar_wait(&empty[s], wrap ^ 1u, p.status, 3)) break;
                 const StageView v = stage_view(smem, p, s);
                 mbar_arrive_expect_tx(&full[s], stage_tx);
                 load_weights<ZP>(v, &tmap_q, &tmap_s, &tmap_z, &full[s], b_lo + issued, n0, p.g_eff);
                 load_acts(v, &tmap_a, &full[s], b_lo + issued);
+                if (++s == p.stages) { s = 0; wrap ^= 1u; }
             }
             // copies still in flight must land before the CTA retires
             for (int i = max(0, issued - p.stages); i < issued; ++i)
@@ -195,7 +207,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
                 for (int e = 0; e < 4; ++e) accg[c][j][e] = 0.f;
         float s0 = 0.f, s1 = 0.f;
         ZeroConst zc0 = make_zero_const<BF16>(8), zc1 = zc0;
-        int cur_g = -1;   // large-group mode: group whose sums accg holds
+        int g_end = -1;   // large-group mode: K where the group whose sums accg holds ends
 
         // acc += scale * group sum.  In the per-group modes the next group's first
         // MMAs overwrite accg (zero accumulator input), so nothing is cleared here.
@@ -223,17 +235,15 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
                 zc1 = make_zero_const<BF16>((v.zp[gl * 16 + (r1 >> 3)] >> (4 * g)) & 0xF);
             }
         };
-        // per-thread shared-memory offsets that do not depend on the stage
-        const int wrow0 = r0 * 128 + (t << 2);     // row r1 = r0 + 8 is 1024 bytes further
-        const int g16 = g << 4;
+        // Per-thread shared-memory offsets that do not depend on the stage.  Word
+        // ws*4 + t of row r0 sits in 16-byte chunk ws ^ (r0 % 8) = ws ^ g (128-byte
+        // swizzle), at byte r0*128 + ((ws ^ g) << 4) + 4t = wofs ^ (ws << 4) with g in
+        // bits 4-6 of wofs; row r1 = r0 + 8 is 1024 bytes further.
+        const int wofs = r0 * 128 + (g << 4) + (t << 2);
         int aoff[NT];
-        bool tok_ok[NT];
 #pragma unroll
-        for (int j = 0; j < NT; ++j) {
-            const int tok = 8 * j + g;
-            aoff[j] = tok * (kBoxK * 2) + (t << 4);   // K-values 8t .. 8t+7 of the word step
-            tok_ok[j] = tok < p.M;
-        }
+        for (int j = 0; j < NT; ++j)
+            aoff[j] = (8 * j + g) * (kBoxK * 2) + (t << 4);   // K-values 8t .. 8t+7 of the word step
 
         // One K box; CHECK: the box may end early at k_hi (the last box of a K range).
         auto run_box = [&](const StageView& v, int box_k, auto check_tag) {
@@ -246,8 +256,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
                 for (int w = 0; w < WPG; ++w) {
                     const int ws = gi * WPG + w;
                     if (CHECK && box_k + ws * 32 >= k_hi) break;
-                    // word ws*4 + t of the box row: 16-byte chunk ws sits at chunk ws ^ (row % 8)
-                    const uint8_t* wp = v.w + wrow0 + ((ws << 4) ^ g16);
+                    const uint8_t* wp = v.w + (wofs ^ (ws << 4));
                     const uint32_t w0 = *reinterpret_cast<const uint32_t*>(wp);
                     const uint32_t w1 = *reinterpret_cast<const uint32_t*>(wp + 1024);
                     uint32_t q0[4], q1[4];
@@ -259,8 +268,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
                     const uint8_t* abox = v.a + ws * 64;
 #pragma unroll
                     for (int j = 0; j < NT; ++j) {
-                        uint4 b = make_uint4(0u, 0u, 0u, 0u);
-                        if (tok_ok[j]) b = *reinterpret_cast<const uint4*>(abox + aoff[j]);
+                        const uint4 b = *reinterpret_cast<const uint4*>(abox + aoff[j]);
                         // step st = 2w + s of the group goes to set st % NSETS; a set's
                         // first step in a group starts from zero (per-group modes)
                         if (WPG < 8 && w == 0) {
@@ -277,24 +285,24 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
             }
         };
 
+        int stage = 0;
+        uint32_t wrap = 0;   // pass over the ring, mod 2: the phase parity to wait for
         for (int i = 0; i < nb; ++i) {
-            const int stage = i % p.stages;
-            const bool got = __all_sync(0xffffffffu,
-                                        mbar_wait(&full[stage], uint32_t(i / p.stages) & 1u, p.status, 1));
+            const bool got = __all_sync(0xffffffffu, mbar_wait(&full[stage], wrap, p.status, 1));
             if (!got) { failed = true; break; }
             const StageView v = stage_view(smem, p, stage);
             const int box_k = (b_lo + i) * kBoxK;
             if constexpr (WPG == 8) {
-                const int grp = box_k / p.g_eff;
-                if (grp != cur_g) {
-                    if (cur_g >= 0) flush();
+                // boxes advance by 256 and a group here spans a multiple of 256 (or all of K)
+                if (box_k >= g_end) {
+                    if (g_end >= 0) flush();
 #pragma unroll
                     for (int c = 0; c < NSETS; ++c)
 #pragma unroll
                         for (int j = 0; j < NT; ++j)
 #pragma unroll
                             for (int e = 0; e < 4; ++e) accg[c][j][e] = 0.f;
-                    cur_g = grp;
+                    g_end = g_end < 0 ? (box_k / p.g_eff + 1) * p.g_eff : g_end + p.g_eff;
                     load_group(v, 0);
                 }
             }
@@ -302,9 +310,10 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
             else run_box(v, box_k, std::true_type{});
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stage]);
+            if (++stage == p.stages) { stage = 0; wrap ^= 1u; }
         }
         if constexpr (WPG == 8) {
-            if (cur_g >= 0) flush();
+            if (g_end >= 0) flush();
         }
     }
 
