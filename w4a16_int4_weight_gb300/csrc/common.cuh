@@ -38,6 +38,35 @@ __device__ __forceinline__ void fence_mbar_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
+// ---------------------------------------------------------------------------
+// Thread-block clusters: split barrier and stores into a peer CTA's shared memory
+// that complete on the peer's mbarrier (no cluster-scope release fence).
+// ---------------------------------------------------------------------------
+// Every thread of every CTA of the cluster arrives; relaxed: orders nothing by
+// itself (mbarrier initialisation is published by fence_mbar_init before it).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait;" ::: "memory");
+}
+
+// Shared-memory address of the same variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t local_smem_addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_smem_addr), "r"(rank));
+    return r;
+}
+
+// 8-byte store into a (possibly remote) CTA's shared memory; its completion is
+// counted as 8 transaction bytes on that CTA's mbarrier `remote_bar`.
+__device__ __forceinline__ void st_async_f32x2(uint32_t remote_addr, float a, float b, uint32_t remote_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];"
+                 ::"r"(remote_addr), "f"(a), "f"(b), "r"(remote_bar)
+                 : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
                  "r"(bytes)

@@ -77,7 +77,7 @@ bool plan_decode(int64_t M, int64_t N, int64_t K, int64_t g_eff, int64_t ng, boo
         const size_t red = ks > 1 ? size_t(kBN) * 8 * nt * 4 : 0;
         for (int st = 1; st <= kMaxPlanStages; ++st) {
             if (st > bp && st > 1) break;
-            const size_t smem = size_t(st) * sb + 128 + red + 1024;
+            const size_t smem = size_t(st) * sb + kBarBytes + red + 1024;
             if (smem > 227 * 1024) break;
             int64_t r = int64_t(228 * 1024) / int64_t(smem + 1024);
             if (r > max_ctas) r = max_ctas;
@@ -137,7 +137,7 @@ cudaError_t launch_decode(const CUtensorMap* maps, void* C, const void* bias, co
     if (p.gps < 1 || p.gps > kMaxGps) return cudaErrorInvalidValue;   // never expected
     p.a_slot = a_slot_for(s.M);
     p.stage_bytes = stage_bytes_for(s.M, p.gps, s.zp);
-    p.red_off = stages * p.stage_bytes + 128;
+    p.red_off = stages * p.stage_bytes + kBarBytes;
     p.prefetch_weights = prefetch_weights ? 1 : 0;
     const int wpg = (s.ng == 1 || s.g_eff >= kBoxK) ? 8 : int(s.g_eff / 32);
     const int grid = int((s.N + kBN - 1) / kBN) * ks;

@@ -7,8 +7,9 @@
 //  * Work split.  A CTA owns 128 weight rows and a contiguous run of 256-wide
 //    K boxes; the KS CTAs that share a row tile form one thread-block cluster
 //    and split K between them.  Their fp32 partials are pushed through
-//    distributed shared memory to the CTA that owns each row, so no global
-//    workspace and no atomics are used.
+//    distributed shared memory to the CTA that owns each row, by stores that
+//    complete on the owner's mbarrier (no cluster-wide release barrier), so
+//    no global workspace and no atomics are used.
 //  * Data movement.  A producer warp streams, per K box and on one mbarrier,
 //    the packed weight box [128 rows x 32 words] (128-byte swizzle), the
 //    activation box [M x 256] (zero-filled past K) and the box's scales and zero
@@ -30,8 +31,6 @@
 //    tolerance; w4a16_dequant keeps the exact per-weight rounding.)
 #pragma once
 
-#include <cooperative_groups.h>
-
 #include <type_traits>
 
 #include "common.cuh"
@@ -40,8 +39,6 @@
 namespace w4a16 {
 namespace decode {
 
-namespace cg = cooperative_groups;
-
 constexpr int kConsumerWarps = 8;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;   // + one producer warp
 constexpr int kBN = 16 * kConsumerWarps;               // weight rows per CTA
@@ -49,6 +46,7 @@ constexpr int kBoxK = 256;               // K-values per box (32 words = 128 byt
 constexpr int kWBytes = kBN * 128;       // 16 KB packed weight box
 constexpr int kMaxStages = 8;
 constexpr int kMaxGps = 8;               // groups per box at G = 32
+constexpr int kBarBytes = 256;           // mbarriers: full[kMaxStages], empty[kMaxStages], red
 
 struct Params {
     uint16_t* C;
@@ -114,6 +112,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
                                                ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.stages * p.stage_bytes);
     uint64_t* empty = full + kMaxStages;
+    uint64_t* red_bar = empty + kMaxStages;   // split K: the partials pushed into this CTA
     float* red = reinterpret_cast<float*>(smem + p.red_off);   // [ks][kBN/ks][MP]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -124,24 +123,26 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     const int nb = b_hi - b_lo;
     const int k_hi = min(p.K, b_hi * kBoxK);
 
-    if (p.M < MP && warp < kConsumerWarps) {
-        // Token rows past M stay zero for the whole kernel: the activation loads
-        // write rows < M only, so the MMA operand loads need no token check.
-        const int row_bytes = kBoxK * 2, pad = (MP - p.M) * row_bytes;
-        for (int s = 0; s < p.stages; ++s) {
-            uint8_t* a = stage_view(smem, p, s).a + p.M * row_bytes;
-            for (int o = tid * 16; o < pad; o += kConsumerWarps * 32 * 16)
-                *reinterpret_cast<uint4*>(a + o) = make_uint4(0u, 0u, 0u, 0u);
-        }
-    }
     if (tid == 0) {
         for (int s = 0; s < kMaxStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kConsumerWarps);
         }
+        mbar_init(red_bar, 1);
         fence_mbar_init();
     }
     __syncthreads();
+    if (p.ks > 1) {
+        // The peers' partials for this CTA's rows: kBN rows x (pairs of token
+        // columns below M) x 8 bytes, whatever the split.  Peers store only after
+        // the cluster barrier, i.e. after every CTA has initialised red_bar.
+        if (tid == 0) {
+            int pairs = 0;
+            for (int j = 0; j < NT; ++j) pairs += min(4, max(0, (p.M - 8 * j + 1) / 2));
+            mbar_arrive_expect_tx(red_bar, uint32_t(kBN * 8 * pairs));
+        }
+        cluster_arrive_relaxed();
+    }
 
     bool failed = false;
     float acc[NT][4];
@@ -240,10 +241,13 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
         // swizzle), at byte r0*128 + ((ws ^ g) << 4) + 4t = wofs ^ (ws << 4) with g in
         // bits 4-6 of wofs; row r1 = r0 + 8 is 1024 bytes further.
         const int wofs = r0 * 128 + (g << 4) + (t << 2);
+        // MMA column g of tile j is token 8j + g.  Columns past M only reach outputs
+        // that are never stored, so their lanes re-read token M - 1 (a broadcast,
+        // and no token check in the loop).
         int aoff[NT];
 #pragma unroll
         for (int j = 0; j < NT; ++j)
-            aoff[j] = (8 * j + g) * (kBoxK * 2) + (t << 4);   // K-values 8t .. 8t+7 of the word step
+            aoff[j] = min(8 * j + g, p.M - 1) * (kBoxK * 2) + (t << 4);   // K-values 8t .. 8t+7 of the step
 
         // One K box; CHECK: the box may end early at k_hi (the last box of a K range).
         auto run_box = [&](const StageView& v, int box_k, auto check_tag) {
@@ -338,26 +342,31 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
         __syncthreads();   // the producer's final waits end before the CTA retires
         return;
     }
-    // Split K: push each partial to the CTA that owns its row, into slot `rank`
-    // of that CTA's reduction buffer, then one cluster barrier.
-    cg::cluster_group cluster = cg::this_cluster();
+    // Split K: each partial goes to the CTA that owns its row, into slot `rank` of
+    // that CTA's reduction buffer, by a store that completes on the owner's
+    // red_bar; an owner waits for its own rows only (no cluster-wide release,
+    // which costs about a microsecond).
     const int rows_per = kBN / p.ks;
+    cluster_wait();   // every CTA's red_bar is initialised
     if (consumer) {
+        const uint32_t red_s = smem_u32(red), bar_s = smem_u32(red_bar);
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
 #pragma unroll
             for (int h = 0; h < 2; ++h) {   // (row, tokens 2t and 2t+1) as one 8-byte store
                 const int tok = 8 * j + 2 * t;
+                if (tok >= p.M) continue;   // columns past M are never summed
                 const int row = h == 0 ? r0 : r1;
                 const int owner = row / rows_per;
-                float* dst = cluster.map_shared_rank(red, owner);
-                *reinterpret_cast<float2*>(dst + (rank * rows_per + (row - owner * rows_per)) * MP + tok) =
-                    make_float2(acc[j][2 * h], acc[j][2 * h + 1]);
+                const uint32_t off = uint32_t(((rank * rows_per + (row - owner * rows_per)) * MP + tok) * 4);
+                st_async_f32x2(cluster_map(red_s + off, uint32_t(owner)), acc[j][2 * h], acc[j][2 * h + 1],
+                               cluster_map(bar_s, uint32_t(owner)));
             }
         }
     }
-    const int any_failed = __syncthreads_or(failed);
-    cluster.sync();
+    // Once red_bar completes no peer writes here any more, so the CTA may retire.
+    const bool got = mbar_wait(red_bar, 0u, p.status, 4);
+    const int any_failed = __syncthreads_or(failed || !got);
     const int items = rows_per * p.M;
     for (int it = tid; it < items; it += kThreads) {
         const int rl = it % rows_per, tok = it / rows_per;
