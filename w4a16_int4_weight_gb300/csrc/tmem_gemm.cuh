@@ -29,18 +29,15 @@
 //
 // Small row counts split K over a thread-block cluster (KS CTAs, whole weight
 // stages each): partial accumulators are pushed through distributed shared
-// memory to the CTA that owns each row block and summed there.
+// memory to the CTA that owns each row block, by stores that complete on that
+// CTA's mbarrier, and summed there.
 #pragma once
-
-#include <cooperative_groups.h>
 
 #include "common.cuh"
 #include "internal.h"
 
 namespace w4a16 {
 namespace tgemm {
-
-namespace cg = cooperative_groups;
 
 constexpr int kBM = 128;                  // weight rows per CTA (UMMA M, TMEM lanes)
 constexpr int kBK = 64;                   // K per MMA block / activation stage / TMEM stage
@@ -103,7 +100,7 @@ struct Layout {
     static constexpr int kBytesNoRed = kRedOff + 1024;
     static constexpr int kBytesRed = kRedOff + kRedBytes + 1024;
     static constexpr bool kSplitFits = kBytesRed <= 227 * 1024;
-    static_assert(2 * (kWStages + kAUnits + kTUnits) * 8 + 8 + 4 <= 512, "barrier area");
+    static_assert(2 * (kWStages + kAUnits + kTUnits) * 8 + 16 + 4 <= 512, "barrier area");
 };
 
 __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
@@ -171,7 +168,8 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BT)) tmem_gemm_kernel(c
     uint64_t* dq_full = a_empty + kAUnits;                               // TMEM unit written
     uint64_t* t_empty = dq_full + kTUnits;                               // MMA done with it
     uint64_t* acc_full = t_empty + kTUnits;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+    uint64_t* red_bar = acc_full + 1;                                    // split K: partials pushed here
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red_bar + 1);
     float* red = reinterpret_cast<float*>(smem + L::kRedOff);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -206,6 +204,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BT)) tmem_gemm_kernel(c
             mbar_init(&t_empty[t], 1);
         }
         mbar_init(acc_full, 1);
+        mbar_init(red_bar, 1);
         fence_mbar_init();
     }
     if (warp == kMmaWarp) {
@@ -215,6 +214,12 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BT)) tmem_gemm_kernel(c
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (p.ks > 1) {
+        // Peers store this CTA's rows of their partial tiles (kBM x BT fp32 in
+        // all) only after the cluster barrier, i.e. after red_bar is initialised.
+        if (tid == 0) mbar_arrive_expect_tx(red_bar, uint32_t(kBM * BT * 4));
+        cluster_arrive_relaxed();
+    }
     const uint32_t tmem = *tmem_slot;
     const uint32_t tmem_d = tmem;                 // accumulator columns [0, BT)
     const uint32_t tmem_a = tmem + BT;            // A stages: 32 columns each
@@ -449,28 +454,34 @@ __global__ void __launch_bounds__(kThreads, min_ctas_for(BT)) tmem_gemm_kernel(c
         if (warp == kMmaWarp) tmem_dealloc(tmem, L::kTmemCols);
         return;
     }
-    // Split K: push the partial tile to the owner of each row block (rows_per rows).
-    cg::cluster_group cluster = cg::this_cluster();
+    // Split K: push the partial tile to the owner of each row block (rows_per rows)
+    // with stores that complete on the owner's red_bar; an owner waits for its own
+    // rows only (a cluster-wide release barrier costs about a microsecond).  Every
+    // row's columns are always sent, zeros after a failed wait, so that red_bar
+    // completes.
     const int rows_per = kBM / p.ks;
-    if (epi && ok) {
+    cluster_wait();   // every CTA's red_bar is initialised
+    if (epi) {
         const int owner = row / rows_per;
-        float* dst = cluster.map_shared_rank(red, owner) + (size_t(rank) * rows_per + (row - owner * rows_per)) * BT;
+        const uint32_t dst = cluster_map(
+            smem_u32(red) + uint32_t((rank * rows_per + (row - owner * rows_per)) * BT * 4), uint32_t(owner));
+        const uint32_t bar = cluster_map(smem_u32(red_bar), uint32_t(owner));
 #pragma unroll 1
         for (int c = 0; c < kColsPerWarp; c += 16) {
             uint32_t r[16] = {};   // a CTA without K blocks contributes zeros
-            if (nkb > 0) {
+            if (ok && nkb > 0) {
                 tmem_ld_32x32b_x16(tmem_d + (uint32_t(32 * (warp & 3)) << 16) + uint32_t(c0 + c), r);
                 tmem_ld_wait();
             }
 #pragma unroll
             for (int j = 0; j < 16; j += 4)
-                *reinterpret_cast<float4*>(dst + c0 + c + j) =
-                    make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
-                                __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+                st_async_f32x4(dst + uint32_t((c0 + c + j) * 4), __uint_as_float(r[j]), __uint_as_float(r[j + 1]),
+                               __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]), bar);
         }
     }
-    const int any_failed = __syncthreads_or(!ok);
-    cluster.sync();
+    // Once red_bar completes no peer writes here any more, so the CTA may retire.
+    const bool got = mbar_wait(red_bar, 0u, p.status, 38);
+    const int any_failed = __syncthreads_or(!ok || !got);
     // this CTA owns rows [rank*rows_per, (rank+1)*rows_per) of the tile
     const int items = rows_per * BT;
     for (int it = tid; it < items; it += kThreads) {
