@@ -68,6 +68,9 @@ def parse():
     ap.add_argument("--profile-case", choices=["decode", "decode_large", "zp", "mid", "prefill", "prefill_smem", "dense", "dequant"],
                     help="only run `--reps` eager launches of one kernel (for ncu), then exit")
     ap.add_argument("--reps", type=int, default=8)
+    ap.add_argument("--sweep", action="store_true",
+                    help="time the 70B-MLP crossover sweep (12 M x 3 group sizes x 2 quant types x 2 dtypes) "
+                         "through the router and print it as a table, then exit")
     return ap.parse_args()
 
 
@@ -400,10 +403,76 @@ def profile_case(args):
     return 0 if code == 0 else 1
 
 
+SWEEP_M = (1, 2, 4, 8, 16, 32, 64, 128, 256, 512, 1024, 4096)
+SWEEP_N, SWEEP_K = 28672, 8192
+
+
+def sweep(args):
+    """Crossover sweep on the 70B MLP shape (K = 8192, N = 28672): every M, group
+    size, quant type and dtype of the workload, each point the routed layer
+    (w4a16_gemm_ex, path AUTO, static weights) on two weight copies (> L2 in
+    all), CUDA-graph replay, CUDA events.  Prints a markdown table."""
+    import torch
+    torch.cuda.set_device(0)
+    from w4a16_int4_weight_gb300 import build as wbuild
+    wbuild.build()
+    from w4a16_int4_weight_gb300 import binding as B
+    from w4a16_int4_weight_gb300 import inputs as synth
+    hbm_peak, tc_peak, _, peak_kind = measured_peaks()
+    N, K, copies = SWEEP_N, SWEEP_K, 2
+    names = {v: k for k, v in B.PATHS.items()}
+    q_dev = [torch.from_numpy(synth.make_weights(synth.Problem(1, N, K, 64, "uint4b8", "bf16", seed=c))[0]).cuda()
+             for c in range(copies)]
+    print(f"Crossover sweep, K = {K}, N = {N}; peaks ({peak_kind}): HBM {hbm_peak:.0f} GB/s, "
+          f"bf16 {tc_peak:.0f} TFLOP/s; t* = max(algorithmic bytes / HBM, 2MNK / bf16 peak)\n")
+    print("| G | qtype | dtype | M | path | us | TFLOP/s | weight GB/s | % HBM | % bf16 | t*/t |")
+    print("|---|---|---|---|---|---|---|---|---|---|---|")
+    for dt in ("bf16", "fp16"):
+        tdt = {"fp16": torch.float16, "bf16": torch.bfloat16}[dt]
+        A = torch.from_numpy(synth.make_activations(
+            synth.Problem(max(SWEEP_M), N, K, 64, "uint4b8", dt, seed=7)).view(np.int16)).cuda().view(tdt)
+        C = torch.empty(max(SWEEP_M), N, dtype=tdt, device="cuda")
+        for G in (-1, 64, 256):
+            for qt in ("uint4b8", "uint4"):
+                tot, so, zo, _ = B.packed_layout(N, K, G, qt, dt)
+                bufs = []
+                for c in range(copies):
+                    p = synth.Problem(1, N, K, G, qt, dt, seed=c)
+                    s = torch.from_numpy(synth.make_scales(p).view(np.int16)).cuda().view(tdt)
+                    z = synth.make_zeros(p)
+                    zd = torch.from_numpy(z).cuda() if z is not None else None
+                    buf = torch.empty(tot, dtype=torch.uint8, device="cuda")
+                    B.pack(q_dev[c], s, zd, buf, N, K, G, qt, dt)
+                    base = buf.data_ptr()
+                    bufs.append((buf, base, base + so, base + zo if zd is not None else None))
+                torch.cuda.synchronize()
+                zp = qt == "uint4"
+                for M in SWEEP_M:
+                    def run():
+                        for (_, wq, sp, zpp) in bufs:
+                            B.gemm_ex(A, wq, sp, zpp, None, C, M, N, K, G, qt, dt, "auto", static_weights=True)
+                    reps = 30 if M <= 64 else 10 if M <= 512 else 3
+                    t = time_graph(torch, run, reps, 2) / copies
+                    fl = 2.0 * M * N * K
+                    ab = alg_bytes(M, N, K, G, zp)
+                    t_star = max(ab / (hbm_peak * 1e9), fl / (tc_peak * 1e12))
+                    print(f"| {G} | {qt} | {dt} | {M} | {names.get(B.route(M, N, K, G, qt, dt), '?')} | "
+                          f"{t * 1e6:.1f} | {fl / t / 1e12:.0f} | {weight_bytes(N, K, G, zp) / t / 1e9:.0f} | "
+                          f"{100 * ab / t / 1e9 / hbm_peak:.0f} | {100 * fl / t / 1e12 / tc_peak:.0f} | "
+                          f"{t_star / t:.2f} |", flush=True)
+                del bufs
+                torch.cuda.empty_cache()
+    code, _ = B.device_status()
+    print(f"\ndevice status {code}")
+    return 0 if code == 0 else 1
+
+
 def main():
     args = parse()
     if args.profile_case:
         return profile_case(args)
+    if args.sweep:
+        return sweep(args)
     if args.impl == "reference":
         world = int(os.environ.get("WORLD_SIZE", "1"))
         rank = int(os.environ.get("RANK", "0"))
