@@ -68,25 +68,27 @@ struct Params {
 };
 
 // Tensor-memory columns per CTA (a power of two for tcgen05.alloc): the
-// accumulator (BT) and a power-of-two number of 32-column A stages, four up to
-// BT = 128 (two CTAs per SM share the 512 columns) and eight at BT = 256.
-constexpr int tmem_cols_for(int bt) { return bt <= 128 ? 256 : 512; }
-constexpr int tmem_stages_for(int bt) { return bt <= 128 ? 4 : 8; }
+// accumulator (BT <= 128 columns) and four 32-column A stages; two CTAs per SM
+// share the 512 columns.
+constexpr int kTmemColsPerCta = 256;
+constexpr int kTmemStagesPerCta = 4;
 
-// Ring depths per token tile: two CTAs per SM up to BT = 128 (one with the
-// split-K buffer at BT >= 64), 96-128 KB of packed weights in flight per SM.
+// Ring depths per token tile (16, 32, 64 or 128 tokens): two CTAs per SM (one
+// with the split-K buffer at BT >= 64), 96-128 KB of packed weights in flight
+// per SM.
 template <int BT>
 struct Layout {
+    static_assert(BT == 16 || BT == 32 || BT == 64 || BT == 128, "token tile");
     // The MMA issuer takes K blocks in units of kUnit = 2: one wait and two
     // commits per unit, which halves its fixed cost per block (a wait costs the
     // single issuing thread 130-220 cycles, a commit ~44; measured faster than
     // one-block units at every token tile, most at 128 tokens: 66 -> 58 us on
-    // the 70B MLP).  Rings sized for two CTAs per SM up to BT = 128.
+    // the 70B MLP).
     static constexpr int kUnit = 2;
-    static constexpr int kWStages = BT <= 32 ? 4 : BT <= 64 ? 3 : BT <= 128 ? 2 : 3;
+    static constexpr int kWStages = BT <= 32 ? 4 : BT <= 64 ? 3 : 2;
     static constexpr int kAUnits = BT <= 16 ? 4 : 2;                  // activation unit-slots
-    static constexpr int kTmemCols = tmem_cols_for(BT);
-    static constexpr int kTmemStages = tmem_stages_for(BT);           // 32-column block stages
+    static constexpr int kTmemCols = kTmemColsPerCta;
+    static constexpr int kTmemStages = kTmemStagesPerCta;             // 32-column block stages
     static constexpr int kTUnits = kTmemStages / kUnit;               // tensor-memory unit-slots
     static_assert(BT + 32 * kTmemStages <= kTmemCols, "tensor-memory budget");
     static_assert((kTmemStages & (kTmemStages - 1)) == 0, "power-of-two tensor-memory ring");
@@ -135,13 +137,12 @@ __device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
         : "memory");
 }
 
-// CTAs per SM the register budget must allow (the launch plan assumes two up
-// to BT = 128).  Three thinner CTAs per SM at BT <= 64 (two weight and two A
-// stages) and splitting 128/256-token tiles over clusters both measured slower.
-constexpr int min_ctas_for(int bt) { return bt <= 128 ? 2 : 1; }
-
+// The register budget allows two CTAs per SM (the launch plan assumes two).
+// Three thinner CTAs per SM at BT <= 64 (two weight and two A stages) and
+// splitting 128-token tiles over clusters both measured slower; so did one CTA
+// per SM with 256-token tiles, at every M up to 4096.
 template <bool BF16, bool ZP, int BT>
-__global__ void __launch_bounds__(kThreads, min_ctas_for(BT)) tmem_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
+__global__ void __launch_bounds__(kThreads, 2) tmem_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                                                 const __grid_constant__ CUtensorMap tmap_w,
                                                                 const __grid_constant__ CUtensorMap tmap_s,
                                                                 const __grid_constant__ CUtensorMap tmap_z,
