@@ -114,6 +114,7 @@ def test_router(B):
     assert B.route(129, 28672, 8192, 64, "uint4", "bf16") == B.PATH_FUSED_TMEM
     assert B.route(2048, 14336, 4096, 128, "uint4b8", "bf16") == B.PATH_FUSED_TMEM
     assert B.route(2048, 14336, 4096, 128, "uint4b8", "bf16", has_dense=True) == B.PATH_DENSE
+    assert B.route(2047, 14336, 4096, 128, "uint4b8", "bf16", has_dense=True) == B.PATH_FUSED_TMEM
     assert B.route(4, 14336, 4096, 128, "uint4b8", "bf16", has_dense=True) == B.PATH_DECODE
     assert B.route(4, 14336, 4100, 128, "uint4b8", "bf16") == -1
 

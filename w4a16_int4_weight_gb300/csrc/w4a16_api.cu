@@ -192,11 +192,14 @@ w4a16_status device_sms(int* sms) {
 // Crossover points measured on GB300 (decode kernel vs the fused tcgen05
 // kernels): decode wins up to M = 16 on every measured layer.  The fused kernel
 // with the dequantised tile in tensor memory beats the one with both operands
-// in shared memory at every measured M (1 .. 2048); the latter stays reachable
+// in shared memory at every measured M (1 .. 4096); the latter stays reachable
 // as W4A16_PATH_FUSED_SMEM.  The dense copy wins over fused dequant only where
-// the tensor pipe, not the dequantisation, limits the fused kernel.
+// the tensor pipe, not the dequantisation, limits the fused kernel: at 1024
+// tokens the fused kernel is level or ahead (14336x4096: 85 vs 91 us; 28672x8192:
+// 313 vs 319 us), from 2048 the dense one mostly leads (28672x8192 M=4096: 1220
+// vs 1325 us).
 constexpr int64_t kDecodeUpToM = 16;
-constexpr int64_t kDenseFromM = 1024;
+constexpr int64_t kDenseFromM = 2048;
 
 int fused_kernel_for(int64_t) { return W4A16_PATH_FUSED_TMEM; }
 
