@@ -157,3 +157,35 @@ def test_pack_ex_rejects_bad_formats(B):
     assert "N divisible by 8" in B.last_error()
     assert B.lib.w4a16_pack_ex(FAKE + 2, 1, FAKE, None, 0, FAKE + 256, 64, 64, 32, 0, 0, None) == B.ERR_INVALID_ARG
     assert "4-byte aligned" in B.last_error()
+
+
+def test_cpython_marshalling_matches_ctypes(B):
+    # the binding's per-call module forwards the same arguments to the same C
+    # functions: identical status and message on every validation outcome
+    if B._fastcall is None:
+        pytest.skip("Python headers unavailable: the binding calls through ctypes only")
+    base = [FAKE, FAKE, FAKE, None, None, FAKE, 4, 256, 4096, 128, 0, 1, 0, None]
+    variants = [
+        {9: 7},                      # group size
+        {8: 4100},                   # K % 16
+        {6: 0},                      # M = 0: no-op, OK without touching the GPU
+        {10: 1},                     # uint4 without zero points
+        {11: 5},                     # dtype
+        {12: 9},                     # path
+        {0: FAKE + 2},               # A alignment
+        {6: -1},                     # negative M
+    ]
+    for v in variants:
+        args = list(base)
+        for i, x in v.items():
+            args[i] = x
+        got = B._gemm_ex_call(*args)
+        msg = B.last_error()
+        want = B.lib.w4a16_gemm_ex(*args)
+        assert got == want, v
+        if want != B.OK:
+            assert B.last_error() == msg, v
+    largs = [FAKE, 0, FAKE, FAKE, None, None, None, FAKE, 0, 4, 256, 4096, 7, 0, 1, 0, None]
+    assert B._linear_call(*largs) == B.lib.w4a16_linear(*largs) == B.ERR_INVALID_ARG
+    with pytest.raises(TypeError):
+        B._gemm_ex_call(*base[:13])

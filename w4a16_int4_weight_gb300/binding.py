@@ -1,4 +1,5 @@
-"""Thin ctypes binding of libw4a16 (C ABI in include/w4a16.h).
+"""Thin binding of libw4a16 (C ABI in include/w4a16.h): ctypes, plus a CPython
+marshalling module for the per-call GEMM entry points.
 
 Argument marshalling only: every entry point forwards raw device pointers,
 sizes and the current CUDA stream to the library, which validates and runs all
@@ -63,6 +64,18 @@ for _name, (_res, _args) in _SIGS.items():
     _f.argtypes = _args
 
 EXPORTED = tuple(_SIGS)
+
+# Per-call entry points: the CPython marshalling module built beside the library
+# (csrc/py_fastcall.c) when the Python headers were available, else ctypes.  Both
+# take the same integer arguments and call the same libw4a16 functions.
+try:
+    from . import _w4a16_fastcall as _fastcall
+    _fastcall.bind(ctypes.cast(lib.w4a16_gemm_ex, ctypes.c_void_p).value,
+                   ctypes.cast(lib.w4a16_linear, ctypes.c_void_p).value)
+    _gemm_ex_call, _linear_call = _fastcall.gemm_ex, _fastcall.linear
+except ImportError:
+    _fastcall = None
+    _gemm_ex_call, _linear_call = lib.w4a16_gemm_ex, lib.w4a16_linear
 
 
 def last_error() -> str:
@@ -156,8 +169,8 @@ def gemm_ex(A, Wq, scales, zeros, Wdense, C, M, N, K, G, qtype, dtype, path="aut
     p = PATHS[path] if isinstance(path, str) else int(path)
     if static_weights:
         p |= OPT_STATIC_WEIGHTS
-    _check(lib.w4a16_gemm_ex(_ptr(A), _ptr(Wq), _ptr(scales), _ptr(zeros), _ptr(Wdense),
-                             _ptr(C), M, N, K, G, _qt(qtype), _dt(dtype), p, _stream(stream)))
+    _check(_gemm_ex_call(_ptr(A), _ptr(Wq), _ptr(scales), _ptr(zeros), _ptr(Wdense),
+                         _ptr(C), M, N, K, G, _qt(qtype), _dt(dtype), p, _stream(stream)))
 
 
 def linear(A, Wq, scales, zeros, bias, Wdense, C, M, N, K, G, qtype, dtype, path="auto",
@@ -167,9 +180,9 @@ def linear(A, Wq, scales, zeros, bias, Wdense, C, M, N, K, G, qtype, dtype, path
     p = PATHS[path] if isinstance(path, str) else int(path)
     if static_weights:
         p |= OPT_STATIC_WEIGHTS
-    _check(lib.w4a16_linear(_ptr(A), lda, _ptr(Wq), _ptr(scales), _ptr(zeros), _ptr(bias),
-                            _ptr(Wdense), _ptr(C), ldc, M, N, K, G, _qt(qtype), _dt(dtype), p,
-                            _stream(stream)))
+    _check(_linear_call(_ptr(A), lda, _ptr(Wq), _ptr(scales), _ptr(zeros), _ptr(bias),
+                        _ptr(Wdense), _ptr(C), ldc, M, N, K, G, _qt(qtype), _dt(dtype), p,
+                        _stream(stream)))
 
 
 QFORMATS = {"unpacked": 0, "gptq": 1, "exllama": 2, "kn": 3}
