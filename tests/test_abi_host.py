@@ -189,3 +189,12 @@ def test_cpython_marshalling_matches_ctypes(B):
     assert B._linear_call(*largs) == B.lib.w4a16_linear(*largs) == B.ERR_INVALID_ARG
     with pytest.raises(TypeError):
         B._gemm_ex_call(*base[:13])
+    # buffers may also be passed as tensors (their data_ptr()); a bad object raises
+    import torch
+    buf = torch.zeros(16, dtype=torch.uint8)
+    targs = [buf, buf, buf, None, None, buf] + base[6:]
+    targs[9] = 7
+    assert B._gemm_ex_call(*targs) == B.ERR_INVALID_ARG and "group size" in B.last_error()
+    targs[1] = object()
+    with pytest.raises(AttributeError):
+        B._gemm_ex_call(*targs)

@@ -169,8 +169,14 @@ def gemm_ex(A, Wq, scales, zeros, Wdense, C, M, N, K, G, qtype, dtype, path="aut
     p = PATHS[path] if isinstance(path, str) else int(path)
     if static_weights:
         p |= OPT_STATIC_WEIGHTS
-    _check(_gemm_ex_call(_ptr(A), _ptr(Wq), _ptr(scales), _ptr(zeros), _ptr(Wdense),
-                         _ptr(C), M, N, K, G, _qt(qtype), _dt(dtype), p, _stream(stream)))
+    if _fastcall is not None:   # takes tensors, int addresses or None as they are
+        code = _fastcall.gemm_ex(A, Wq, scales, zeros, Wdense, C, M, N, K, G, _qt(qtype), _dt(dtype),
+                                 p, _stream(stream))
+    else:
+        code = lib.w4a16_gemm_ex(_ptr(A), _ptr(Wq), _ptr(scales), _ptr(zeros), _ptr(Wdense), _ptr(C),
+                                 M, N, K, G, _qt(qtype), _dt(dtype), p, _stream(stream))
+    if code:
+        raise W4A16Error(code, last_error())
 
 
 def linear(A, Wq, scales, zeros, bias, Wdense, C, M, N, K, G, qtype, dtype, path="auto",
@@ -180,9 +186,10 @@ def linear(A, Wq, scales, zeros, bias, Wdense, C, M, N, K, G, qtype, dtype, path
     p = PATHS[path] if isinstance(path, str) else int(path)
     if static_weights:
         p |= OPT_STATIC_WEIGHTS
-    _check(_linear_call(_ptr(A), lda, _ptr(Wq), _ptr(scales), _ptr(zeros), _ptr(bias),
-                        _ptr(Wdense), _ptr(C), ldc, M, N, K, G, _qt(qtype), _dt(dtype), p,
-                        _stream(stream)))
+    call = _fastcall.linear if _fastcall is not None else lib.w4a16_linear
+    _check(call(_ptr(A), lda, _ptr(Wq), _ptr(scales), _ptr(zeros), _ptr(bias),
+                _ptr(Wdense), _ptr(C), ldc, M, N, K, G, _qt(qtype), _dt(dtype), p,
+                _stream(stream)))
 
 
 QFORMATS = {"unpacked": 0, "gptq": 1, "exllama": 2, "kn": 3}

@@ -23,11 +23,19 @@ typedef int (*linear_fn)(const void* A, int64_t lda, const void* Wq, const void*
 
 static gemm_ex_fn g_gemm_ex = NULL;
 static linear_fn g_linear = NULL;
+static PyObject* g_data_ptr = NULL;   /* interned "data_ptr" */
 
-/* None -> NULL; an int -> that address. */
+/* None -> NULL; an int -> that address; any other object (a torch tensor) ->
+   the address its data_ptr() method returns. */
 static void* as_ptr(PyObject* o) {
     if (o == Py_None) return NULL;
-    return PyLong_AsVoidPtr(o);
+    if (PyLong_Check(o)) return PyLong_AsVoidPtr(o);
+    if (PyErr_Occurred()) return NULL;   /* an earlier argument failed: call nothing more */
+    PyObject* r = PyObject_CallMethodNoArgs(o, g_data_ptr);
+    if (!r) return NULL;
+    void* p = PyLong_AsVoidPtr(r);
+    Py_DECREF(r);
+    return p;
 }
 
 static int as_int(PyObject* o) { return (int)PyLong_AsLong(o); }
@@ -107,13 +115,17 @@ static PyObject* fc_linear(PyObject* self, PyObject* const* a, Py_ssize_t n) {
 static PyMethodDef fc_methods[] = {
     {"bind", fc_bind, METH_VARARGS, "bind(gemm_ex_address, linear_address)"},
     {"gemm_ex", (PyCFunction)(void (*)(void))fc_gemm_ex, METH_FASTCALL,
-     "w4a16_gemm_ex with integer addresses and sizes; returns the status code"},
+     "w4a16_gemm_ex; buffers as None, int addresses or tensors (data_ptr()); returns the status code"},
     {"linear", (PyCFunction)(void (*)(void))fc_linear, METH_FASTCALL,
-     "w4a16_linear with integer addresses and sizes; returns the status code"},
+     "w4a16_linear; buffers as None, int addresses or tensors (data_ptr()); returns the status code"},
     {NULL, NULL, 0, NULL},
 };
 
 static struct PyModuleDef fc_module = {PyModuleDef_HEAD_INIT, "_w4a16_fastcall", NULL, -1, fc_methods,
                                        NULL, NULL, NULL, NULL};
 
-PyMODINIT_FUNC PyInit__w4a16_fastcall(void) { return PyModule_Create(&fc_module); }
+PyMODINIT_FUNC PyInit__w4a16_fastcall(void) {
+    g_data_ptr = PyUnicode_InternFromString("data_ptr");
+    if (!g_data_ptr) return NULL;
+    return PyModule_Create(&fc_module);
+}
