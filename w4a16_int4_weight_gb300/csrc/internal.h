@@ -73,10 +73,11 @@ cudaError_t launch_prefill(const CUtensorMap* maps, void* C, const void* bias, c
 // tmem_gemm.cu: fused-dequant tcgen05 GEMM with the weight tile in tensor memory.
 // maps: A [M][K] box {64, BT} SW128 (BT = tmem_gemm_token_tile(M)); packed
 // [N][ldq] box {32,128} SW128; scales [ng][lds] box {128, gps}; zeros [ng][ldz]
-// box {16, gps}, gps = decode_scale_box_rows(g_eff, ng).
+// box {16, gps}, gps = decode_scale_box_rows(g_eff, ng); maps[4]: C [M][N] box {128, BT},
+// valid when c_tma (16-byte aligned base and row pitch).
 int tmem_gemm_token_tile(int64_t M);
 cudaError_t launch_tmem_gemm(const CUtensorMap* maps, void* C, const void* bias, const LayerShape& s,
-                             int num_sms, bool prefetch_weights, cudaStream_t stream);
+                             int num_sms, bool prefetch_weights, bool c_tma, cudaStream_t stream);
 int take_status_tmem_gemm();
 
 // Status words of each module: read-and-clear (synchronous).

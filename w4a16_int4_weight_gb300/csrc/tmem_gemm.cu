@@ -57,7 +57,7 @@ cudaError_t launch_t(const CUtensorMap* maps, const tgemm::Params& p, int grid_x
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], p);
+    return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], p);
 }
 
 template <int BT>
@@ -132,7 +132,7 @@ int tmem_gemm_ksplit(int64_t M, int64_t N, int64_t K, int num_sms) {
 }
 
 cudaError_t launch_tmem_gemm(const CUtensorMap* maps, void* C, const void* bias, const LayerShape& s,
-                             int num_sms, bool prefetch_weights, cudaStream_t stream) {
+                             int num_sms, bool prefetch_weights, bool c_tma, cudaStream_t stream) {
     tgemm::Params p;
     p.C = static_cast<uint16_t*>(C);
     p.bias = static_cast<const uint16_t*>(bias);
@@ -149,6 +149,7 @@ cudaError_t launch_tmem_gemm(const CUtensorMap* maps, void* C, const void* bias,
     p.gps = decode_scale_box_rows(p.g_eff, p.ng);
     p.ks = tmem_gemm_ksplit(s.M, s.N, s.K, num_sms);
     p.prefetch_weights = prefetch_weights ? 1 : 0;
+    p.c_tma = c_tma ? 1 : 0;
     const int bt = tmem_gemm_token_tile(s.M);
     const int64_t ctas = ((s.N + tgemm::kBM - 1) / tgemm::kBM) * ((s.M + bt - 1) / bt) * p.ks;
     if (ctas > int64_t(0x7fffffff)) return cudaErrorInvalidValue;   // beyond any C that fits in memory

@@ -65,6 +65,8 @@ struct Params {
     int nws;           // ceil(K / kWK) weight stages
     int ks;            // CTAs per cluster (K split); 1 = whole K per CTA
     int prefetch_weights;
+    int c_tma;         // tmap_c describes C (16-byte aligned base and row pitch): whole-K tiles
+                       // leave through one TMA store of a shared-memory tile
 };
 
 // Tensor-memory columns per CTA (a power of two for tcgen05.alloc): the
@@ -146,6 +148,7 @@ __global__ void __launch_bounds__(kThreads, 2) tmem_gemm_kernel(const __grid_con
                                                                 const __grid_constant__ CUtensorMap tmap_w,
                                                                 const __grid_constant__ CUtensorMap tmap_s,
                                                                 const __grid_constant__ CUtensorMap tmap_z,
+                                                                const __grid_constant__ CUtensorMap tmap_c,
                                                                 const Params p) {
     using L = Layout<BT>;
     constexpr int kWStages = L::kWStages;
@@ -432,6 +435,39 @@ __global__ void __launch_bounds__(kThreads, 2) tmem_gemm_kernel(const __grid_con
     const int c0 = (warp >> 2) * kColsPerWarp;
     // the bias of an output row, 0 without one
     auto bias_of = [&](int n) { return p.bias && n < p.N ? to_f32<BF16>(p.bias[n]) : 0.f; };
+    if (p.ks == 1 && p.c_tma) {
+        // Stage the output tile [BT tokens][128 rows] in the dtype in the activation
+        // ring (the tensor core's last reads of it completed before acc_full), then
+        // one TMA store; it clips rows >= N and tokens >= M.  Two-byte stores of
+        // 32 lanes straight to global memory took ~2 us of a 27 us tile.
+        static_assert(L::kAUnits * L::kAUnitBytes >= BT * kBM * 2, "output tile fits the activation ring");
+        uint16_t* stg = reinterpret_cast<uint16_t*>(smem + L::kActOff);
+        if (epi) {
+            if (ok && nkb > 0) {
+                const float b = bias_of(n0 + row);
+#pragma unroll 1
+                for (int c = 0; c < kColsPerWarp; c += 16) {
+                    uint32_t r[16];
+                    tmem_ld_32x32b_x16(tmem_d + (uint32_t(32 * (warp & 3)) << 16) + uint32_t(c0 + c), r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        stg[(c0 + c + j) * kBM + row] = from_f32<BF16>(__uint_as_float(r[j]) + b);
+                }
+                fence_proxy_async_smem();
+            }
+            named_barrier_sync(1, 4 * kHalves * 32);
+            if (warp == 0 && lane == 0 && ok && nkb > 0) {
+                tma_store_2d(&tmap_c, stg, n0, m0);
+                bulk_commit_group();
+                bulk_wait_read_all();   // the tile must stay until the store has read it
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+        if (warp == kMmaWarp) tmem_dealloc(tmem, L::kTmemCols);
+        return;
+    }
     if (p.ks == 1) {
         if (epi && ok && nkb > 0) {
             const int n = n0 + row;

@@ -269,7 +269,7 @@ w4a16_status launch_tmem_path(const void* A, const void* Wq, const void* scales,
     const int bt = tmem_gemm_token_tile(s.M);
     // weight stages of 256 K-values: 128-byte packed rows and the group rows they span
     const uint32_t gps = uint32_t(decode_scale_box_rows(s.g_eff, s.ng));
-    CUtensorMap maps[4];
+    CUtensorMap maps[5];
     st = make_map(&maps[0], A, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, uint64_t(s.K), uint64_t(s.M),
                   uint64_t(s.lda) * 2, 64, uint32_t(bt), CU_TENSOR_MAP_SWIZZLE_128B);
     if (st) return st;
@@ -286,7 +286,16 @@ w4a16_status launch_tmem_path(const void* A, const void* Wq, const void* scales,
     } else {
         maps[3] = maps[2];   // unused without zero points
     }
-    cudaError_t e = launch_tmem_gemm(maps, C, bias, s, sms, static_weights, stream);
+    // the output leaves by TMA store when its base and row pitch are 16-byte aligned
+    const bool c_tma = (reinterpret_cast<uintptr_t>(C) & 15) == 0 && (s.ldc * 2) % 16 == 0;
+    if (c_tma) {
+        st = make_map(&maps[4], C, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, uint64_t(s.N), uint64_t(s.M),
+                      uint64_t(s.ldc) * 2, 128, uint32_t(bt), CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (st) return st;
+    } else {
+        maps[4] = maps[0];   // unused
+    }
+    cudaError_t e = launch_tmem_gemm(maps, C, bias, s, sms, static_weights, c_tma, stream);
     if (e != cudaSuccess) return cuda_fail(e, "tensor-memory GEMM launch");
     return W4A16_OK;
 }
