@@ -68,7 +68,7 @@ bool plan_decode(int64_t M, int64_t N, int64_t K, int64_t g_eff, int64_t ng, boo
 // maps: A [M][K] box {64,BT} SW128; weights (packed [N][ldq] box {8,128} SW32, or
 // dense [N][K] box {64,128} SW128); scales [ng][lds] box {128,2}; zeros [ng][ldz] box {16,2}.
 cudaError_t launch_prefill(const CUtensorMap* maps, void* C, const void* bias, const LayerShape& s, bool dense,
-                           int token_tile, cudaStream_t stream);
+                           int token_tile, bool c_tma, cudaStream_t stream);   // maps[4]: C, when c_tma
 
 // tmem_gemm.cu: fused-dequant tcgen05 GEMM with the weight tile in tensor memory.
 // maps: A [M][K] box {64, BT} SW128 (BT = tmem_gemm_token_tile(M)); packed

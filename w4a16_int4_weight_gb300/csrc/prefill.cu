@@ -49,6 +49,7 @@ struct Params {
     int64_t ldc;            // row pitch of C in elements (>= N)
     int M, N, K, g_eff, ng;
     int nkb;   // ceil(K / kBK)
+    int c_tma; // tmap_c describes C (16-byte aligned base and row pitch): the tile leaves by TMA store
 };
 
 template <int BT, bool DENSE>
@@ -65,6 +66,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                                                               const __grid_constant__ CUtensorMap tmap_w,
                                                               const __grid_constant__ CUtensorMap tmap_s,
                                                               const __grid_constant__ CUtensorMap tmap_z,
+                                                              const __grid_constant__ CUtensorMap tmap_c,
                                                               const Params p) {
     using L = Layout<BT, DENSE>;
     extern __shared__ uint8_t smem_raw[];
@@ -209,7 +211,35 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         if (ok) ok = mbar_wait(acc_full, 0u, p_status(), 15);
         ok = __all_sync(0xffffffffu, ok);   // tcgen05.ld below is warp-collective
         tc_fence_after();
-        if (ok) {
+        if (p.c_tma) {
+            // Stage the output tile [BT tokens][128 rows] in the dtype in the operand
+            // ring (the tensor core's reads of it completed before acc_full), then one
+            // TMA store that clips rows >= N and tokens >= M.
+            static_assert(kStages * L::kStageBytes >= BT * kBM * 2, "output tile fits the operand ring");
+            uint16_t* stg = reinterpret_cast<uint16_t*>(smem);
+            if (ok) {
+                const uint32_t lane_base = uint32_t(32 * (warp & 3)) << 16;
+                const int rl = 32 * (warp & 3) + lane;
+                const int n_out = n0 + rl;
+                const float b = p.bias && n_out < p.N ? to_f32<BF16>(p.bias[n_out]) : 0.f;
+#pragma unroll 1
+                for (int c = (warp >> 2) * (BT / 64); c < ((warp >> 2) + 1) * (BT / 64); ++c) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(tmem_d + lane_base + uint32_t(32 * c), r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        stg[(32 * c + j) * kBM + rl] = from_f32<BF16>(__uint_as_float(r[j]) + b);
+                }
+                fence_proxy_async_smem();
+            }
+            named_barrier_sync(1, kDqWarps * 32);
+            if (warp == 0 && lane == 0 && ok) {
+                tma_store_2d(&tmap_c, stg, n0, m0);
+                bulk_commit_group();
+                bulk_wait_read_all();   // the tile must stay until the store has read it
+            }
+        } else if (ok) {
             // warp w reads TMEM lanes 32*(w%4).. (its rows) and half w/4 of the columns
             const uint32_t lane_base = uint32_t(32 * (warp & 3)) << 16;
             const int n_out = n0 + 32 * (warp & 3) + lane;
@@ -245,7 +275,7 @@ cudaError_t launch_t(const CUtensorMap* maps, const Params& p, cudaStream_t stre
     const int64_t ctas = int64_t((p.N + kBM - 1) / kBM) * ((p.M + BT - 1) / BT);
     if (ctas > int64_t(0x7fffffff)) return cudaErrorInvalidValue;   // beyond any C that fits in memory
     const dim3 grid(static_cast<unsigned>(ctas));
-    kern<<<grid, kThreads, smem, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
+    kern<<<grid, kThreads, smem, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p);
     return cudaGetLastError();
 }
 
@@ -263,8 +293,9 @@ cudaError_t launch_bt(const CUtensorMap* maps, const Params& p, bool bf16, bool 
 }  // namespace
 
 cudaError_t launch_prefill(const CUtensorMap* maps, void* C, const void* bias, const LayerShape& s, bool dense,
-                           int token_tile, cudaStream_t stream) {
+                           int token_tile, bool c_tma, cudaStream_t stream) {
     Params p;
+    p.c_tma = c_tma ? 1 : 0;
     p.C = static_cast<uint16_t*>(C);
     p.bias = static_cast<const uint16_t*>(bias);
     p.ldc = s.ldc;

@@ -229,7 +229,7 @@ w4a16_status launch_tcgen05(const void* A, const void* Wsrc, bool dense, const v
                             const int32_t* zeros, const void* bias, void* C, const LayerShape& s,
                             cudaStream_t stream) {
     const int bt = token_tile_for(s.M);
-    CUtensorMap maps[4];
+    CUtensorMap maps[5];
     w4a16_status st = make_map(&maps[0], A, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, uint64_t(s.K),
                                uint64_t(s.M), uint64_t(s.lda) * 2, 64, uint32_t(bt),
                                CU_TENSOR_MAP_SWIZZLE_128B);
@@ -255,7 +255,16 @@ w4a16_status launch_tcgen05(const void* A, const void* Wsrc, bool dense, const v
             maps[3] = maps[2];   // unused without zero points
         }
     }
-    cudaError_t e = launch_prefill(maps, C, bias, s, dense, bt, stream);
+    // the output leaves by TMA store when its base and row pitch are 16-byte aligned
+    const bool c_tma = (reinterpret_cast<uintptr_t>(C) & 15) == 0 && (s.ldc * 2) % 16 == 0;
+    if (c_tma) {
+        st = make_map(&maps[4], C, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, uint64_t(s.N), uint64_t(s.M),
+                      uint64_t(s.ldc) * 2, 128, uint32_t(bt), CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (st) return st;
+    } else {
+        maps[4] = maps[0];   // unused
+    }
+    cudaError_t e = launch_prefill(maps, C, bias, s, dense, bt, c_tma, stream);
     if (e != cudaSuccess) return cuda_fail(e, "tcgen05 GEMM launch");
     return W4A16_OK;
 }
