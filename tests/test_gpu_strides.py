@@ -46,3 +46,28 @@ def test_padded_a_and_c(sh):
         if ldc > N:
             assert torch.all(C_wide[:, N:] == 7.0), path
     assert_device_status_ok()
+
+
+@pytest.mark.parametrize("path", ["fused_tmem", "fused_smem", "dense"])
+def test_c_base_off_sixteen_byte_alignment(path):
+    # C starts one element into its buffer: the tcgen05 kernels must take their
+    # direct-store epilogue (no TMA store) and still write exactly [M, N].
+    M, N, K, G, qt, dt = 130, 264, 1024, 128, "uint4b8", "bf16"
+    p = synth.Problem(M, N, K, G, qt, dt)
+    x = synth.make_inputs(p)
+    C_ref = orc.linear(x.A, x.q, x.scales, x.zeros, G, dt)
+    w = DeviceWeight(p, x.q, x.scales, x.zeros)
+    ldc = N + 8
+    buf = torch.full((M + 1, ldc), 7.0, dtype=TORCH[dt], device="cuda")
+    flat = buf.view(-1)
+    C = flat[1:1 + M * ldc].view(M, ldc)          # base address 2 bytes past a 16-byte boundary
+    assert C.data_ptr() % 16 == 2
+    A = to_dev_bits(x.A, dt)
+    B().linear(A, w.Wq, w.scales, w.zeros, None, w.dequant() if path == "dense" else None,
+               C, M, N, K, G, qt, dt, path, ldc=ldc)
+    torch.cuda.synchronize()
+    got = to_host_bits(C[:, :N])
+    assert orc.rel_error(orc.values(got, dt), C_ref) <= TOL[dt]
+    assert torch.all(C[:, N:] == 7.0) and float(flat[0]) == 7.0
+    assert torch.all(flat[1 + M * ldc:] == 7.0)
+    assert_device_status_ok()
