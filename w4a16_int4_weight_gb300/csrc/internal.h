@@ -84,4 +84,10 @@ int take_status_tmem_gemm();
 int take_status_decode();
 int take_status_prefill();
 
+// dense_gemm.cu: persistent dense-copy GEMM (one CTA per SM, two tensor-memory
+// accumulators).  maps: A [M][K] box {64, 256} SW128; dense weight [N][K] box {64, 128} SW128.
+cudaError_t launch_dense_gemm(const CUtensorMap* maps, void* C, const void* bias, const LayerShape& s,
+                              int num_sms, cudaStream_t stream);
+int take_status_dense();
+
 }  // namespace w4a16

@@ -228,6 +228,22 @@ int token_tile_for(int64_t M) {
 w4a16_status launch_tcgen05(const void* A, const void* Wsrc, bool dense, const void* scales,
                             const int32_t* zeros, const void* bias, void* C, const LayerShape& s,
                             cudaStream_t stream) {
+    if (dense) {
+        // persistent dense-copy GEMM: 256-token tiles, one CTA per SM
+        int sms = 0;
+        w4a16_status st = device_sms(&sms);
+        if (st) return st;
+        CUtensorMap maps[2];
+        st = make_map(&maps[0], A, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, uint64_t(s.K), uint64_t(s.M),
+                      uint64_t(s.lda) * 2, 64, 256, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (st) return st;
+        st = make_map(&maps[1], Wsrc, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, uint64_t(s.K), uint64_t(s.N),
+                      uint64_t(s.K) * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (st) return st;
+        cudaError_t e = launch_dense_gemm(maps, C, bias, s, sms, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "dense GEMM launch");
+        return W4A16_OK;
+    }
     const int bt = token_tile_for(s.M);
     CUtensorMap maps[5];
     w4a16_status st = make_map(&maps[0], A, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, uint64_t(s.K),
@@ -522,6 +538,7 @@ w4a16_status w4a16_device_status(int* site) {
     int v = take_status_decode();
     if (v == 0) v = take_status_prefill();
     if (v == 0) v = take_status_tmem_gemm();
+    if (v == 0) v = take_status_dense();
     if (site) *site = v > 0 ? v : 0;
     if (v < 0) return fail(W4A16_ERR_CUDA, "reading the device status word failed");
     if (v > 0) return fail(W4A16_ERR_DEVICE_TIMEOUT, "a kernel barrier wait timed out at site %d", v);
