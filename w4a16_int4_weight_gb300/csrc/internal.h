@@ -64,10 +64,10 @@ int decode_scale_box_rows(int64_t g_eff, int64_t ng);
 bool plan_decode(int64_t M, int64_t N, int64_t K, int64_t g_eff, int64_t ng, bool zp,
                  int num_sms, int* ks_out, int* stages_out, size_t* smem_out, int* nt_out);
 
-// prefill.cu: tcgen05 GEMM, fused-dequant (Wq != null) or dense (tmap_w dense).
-// maps: A [M][K] box {64,BT} SW128; weights (packed [N][ldq] box {8,128} SW32, or
-// dense [N][K] box {64,128} SW128); scales [ng][lds] box {128,2}; zeros [ng][ldz] box {16,2}.
-cudaError_t launch_prefill(const CUtensorMap* maps, void* C, const void* bias, const LayerShape& s, bool dense,
+// prefill.cu: fused-dequant tcgen05 GEMM with the dequantised tile in shared memory.
+// maps: A [M][K] box {64,BT} SW128; packed [N][ldq] box {8,128} SW32; scales [ng][lds]
+// box {128,2}; zeros [ng][ldz] box {16,2}.
+cudaError_t launch_prefill(const CUtensorMap* maps, void* C, const void* bias, const LayerShape& s,
                            int token_tile, bool c_tma, cudaStream_t stream);   // maps[4]: C, when c_tma
 
 // tmem_gemm.cu: fused-dequant tcgen05 GEMM with the weight tile in tensor memory.

@@ -6,11 +6,10 @@
 // algebra runs as a warp-specialised tcgen05 pipeline:
 //
 //   warp 8     TMA producer: per 64-wide K block, the activation tile
-//              [BT tokens x 64] (128-byte swizzle) and either the packed weight
-//              tile [128 rows x 8 words] (32-byte swizzle) with its scale and
-//              zero-point rows (fused), or the dense weight tile [128 x 64]
-//              (dense path), into a 4-stage ring.
-//   warps 0-7  dequantisers (fused path): thread i owns half of weight row
+//              [BT tokens x 64] (128-byte swizzle) and the packed weight tile
+//              [128 rows x 8 words] (32-byte swizzle) with its scale and
+//              zero-point rows, into a 4-stage ring.
+//   warps 0-7  dequantisers: thread i owns half of weight row
 //              i % 128 (32 K-values), unpacks with LOP3 magic-number unpacks,
 //              forms rne((q - z) * s) exactly as the pages do, and stores the
 //              bf16/fp16 tile in the 128-byte-swizzled K-major layout the tensor
@@ -35,7 +34,7 @@ constexpr int kDqWarps = 8;               // dequantiser / epilogue warps
 constexpr int kProducerWarp = kDqWarps;
 constexpr int kMmaWarp = kDqWarps + 1;
 constexpr int kThreads = (kDqWarps + 2) * 32;
-constexpr int kWtBytes = kBM * 128;       // 16 KB dequantised / dense weight tile
+constexpr int kWtBytes = kBM * 128;       // 16 KB dequantised weight tile
 constexpr int kPkBytes = kBM * 32;        // 4 KB packed tile (8 words per row)
 constexpr int kScBytes = 2 * kBM * 2;     // scales of two groups x 128 rows
 constexpr int kZpBytes = 2 * 16 * 4;      // zero-point words of two groups x 128 rows
@@ -52,23 +51,23 @@ struct Params {
     int c_tma; // tmap_c describes C (16-byte aligned base and row pitch): the tile leaves by TMA store
 };
 
-template <int BT, bool DENSE>
+template <int BT>
 struct Layout {
     static constexpr int kActBytes = BT * 128;
     static constexpr int kStageBytes =
-        (kActBytes + kWtBytes + (DENSE ? 0 : kPkBytes + kScBytes + kZpBytes) + 1023) / 1024 * 1024;
+        (kActBytes + kWtBytes + kPkBytes + kScBytes + kZpBytes + 1023) / 1024 * 1024;
     static constexpr int kBarOff = kStages * kStageBytes;
     static constexpr int kBytes = kBarOff + 256 + 1024;   // + barriers, + alignment slack
 };
 
-template <bool BF16, bool ZP, int BT, bool DENSE>
+template <bool BF16, bool ZP, int BT>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                                               const __grid_constant__ CUtensorMap tmap_w,
                                                               const __grid_constant__ CUtensorMap tmap_s,
                                                               const __grid_constant__ CUtensorMap tmap_z,
                                                               const __grid_constant__ CUtensorMap tmap_c,
                                                               const Params p) {
-    using L = Layout<BT, DENSE>;
+    using L = Layout<BT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -125,18 +124,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 if (kb >= kStages)
                     ok = mbar_wait(&empty[s], uint32_t(kb / kStages - 1) & 1u, p_status(), 10);
                 if (!ok) break;
-                mbar_arrive_expect_tx(&full[s], L::kActBytes + (DENSE ? kWtBytes
-                                                     : kPkBytes + kScBytes + (ZP ? kZpBytes : 0)));
+                mbar_arrive_expect_tx(&full[s], L::kActBytes + kPkBytes + kScBytes + (ZP ? kZpBytes : 0));
                 tma_load_2d(act_tile(s), &tmap_a, &full[s], kb * kBK, m0);
-                if constexpr (DENSE) {
-                    tma_load_2d(wt_tile(s), &tmap_w, &full[s], kb * kBK, n0);
-                } else {
-                    // the K block's first group and the one after it (used when G = 32)
-                    const int g0 = (kb * kBK) / p.g_eff;
-                    tma_load_2d(pk_tile(s), &tmap_w, &full[s], kb * (kBK / 8), n0);
-                    tma_load_2d(sc_tile(s), &tmap_s, &full[s], n0, g0);
-                    if constexpr (ZP) tma_load_2d(zp_tile(s), &tmap_z, &full[s], n0 / 8, g0);
-                }
+                // the K block's first group and the one after it (used when G = 32)
+                const int g0 = (kb * kBK) / p.g_eff;
+                tma_load_2d(pk_tile(s), &tmap_w, &full[s], kb * (kBK / 8), n0);
+                tma_load_2d(sc_tile(s), &tmap_s, &full[s], n0, g0);
+                if constexpr (ZP) tma_load_2d(zp_tile(s), &tmap_z, &full[s], n0 / 8, g0);
                 ++issued;
             }
             // copies still in flight must land before the CTA can retire
@@ -152,7 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 const int s = kb % kStages;
                 const uint32_t par = uint32_t(kb / kStages) & 1u;
                 ok = mbar_wait(&full[s], par, p_status(), 12);
-                if (ok && !DENSE) ok = mbar_wait(&dq_full[s], par, p_status(), 13);
+                if (ok) ok = mbar_wait(&dq_full[s], par, p_status(), 13);
                 if (!ok) break;
                 tc_fence_after();
                 const uint64_t a_desc = smem_desc_sw128(wt_tile(s));
@@ -169,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         const int row = tid & (kBM - 1);     // weight row within the tile
         const int half = tid >> 7;           // K-values 32*half .. +31 of each block
         bool ok = true;
-        if constexpr (!DENSE) {
+        {
             for (int kb = 0; kb < p.nkb; ++kb) {
                 const int s = kb % kStages;
                 // warp-uniform outcome: the warp leaves the loop together or not at all
@@ -266,10 +260,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     if (warp == kMmaWarp) tmem_dealloc(tmem_d, BT);
 }
 
-template <bool BF16, bool ZP, int BT, bool DENSE>
+template <bool BF16, bool ZP, int BT>
 cudaError_t launch_t(const CUtensorMap* maps, const Params& p, cudaStream_t stream) {
-    auto kern = prefill_kernel<BF16, ZP, BT, DENSE>;
-    constexpr int smem = Layout<BT, DENSE>::kBytes;
+    auto kern = prefill_kernel<BF16, ZP, BT>;
+    constexpr int smem = Layout<BT>::kBytes;
     cudaError_t e = ensure_smem(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
     const int64_t ctas = int64_t((p.N + kBM - 1) / kBM) * ((p.M + BT - 1) / BT);
@@ -280,19 +274,14 @@ cudaError_t launch_t(const CUtensorMap* maps, const Params& p, cudaStream_t stre
 }
 
 template <int BT>
-cudaError_t launch_bt(const CUtensorMap* maps, const Params& p, bool bf16, bool zp, bool dense,
-                      cudaStream_t stream) {
-    if (dense) return bf16 ? launch_t<true, false, BT, true>(maps, p, stream)
-                           : launch_t<false, false, BT, true>(maps, p, stream);
-    if (bf16) return zp ? launch_t<true, true, BT, false>(maps, p, stream)
-                        : launch_t<true, false, BT, false>(maps, p, stream);
-    return zp ? launch_t<false, true, BT, false>(maps, p, stream)
-              : launch_t<false, false, BT, false>(maps, p, stream);
+cudaError_t launch_bt(const CUtensorMap* maps, const Params& p, bool bf16, bool zp, cudaStream_t stream) {
+    if (bf16) return zp ? launch_t<true, true, BT>(maps, p, stream) : launch_t<true, false, BT>(maps, p, stream);
+    return zp ? launch_t<false, true, BT>(maps, p, stream) : launch_t<false, false, BT>(maps, p, stream);
 }
 
 }  // namespace
 
-cudaError_t launch_prefill(const CUtensorMap* maps, void* C, const void* bias, const LayerShape& s, bool dense,
+cudaError_t launch_prefill(const CUtensorMap* maps, void* C, const void* bias, const LayerShape& s,
                            int token_tile, bool c_tma, cudaStream_t stream) {
     Params p;
     p.c_tma = c_tma ? 1 : 0;
@@ -306,9 +295,9 @@ cudaError_t launch_prefill(const CUtensorMap* maps, void* C, const void* bias, c
     p.ng = int(s.ng);
     p.nkb = int((s.K + kBK - 1) / kBK);
     switch (token_tile) {
-        case 64: return launch_bt<64>(maps, p, s.bf16, s.zp, dense, stream);
-        case 128: return launch_bt<128>(maps, p, s.bf16, s.zp, dense, stream);
-        default: return launch_bt<256>(maps, p, s.bf16, s.zp, dense, stream);
+        case 64: return launch_bt<64>(maps, p, s.bf16, s.zp, stream);
+        case 128: return launch_bt<128>(maps, p, s.bf16, s.zp, stream);
+        default: return launch_bt<256>(maps, p, s.bf16, s.zp, stream);
     }
 }
 

@@ -250,13 +250,7 @@ w4a16_status launch_tcgen05(const void* A, const void* Wsrc, bool dense, const v
                                uint64_t(s.M), uint64_t(s.lda) * 2, 64, uint32_t(bt),
                                CU_TENSOR_MAP_SWIZZLE_128B);
     if (st) return st;
-    if (dense) {
-        st = make_map(&maps[1], Wsrc, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, uint64_t(s.K), uint64_t(s.N),
-                      uint64_t(s.K) * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
-        if (st) return st;
-        maps[2] = maps[0];   // unused by the dense kernel
-        maps[3] = maps[0];
-    } else {
+    {
         st = make_map(&maps[1], Wsrc, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, uint64_t(s.ldq), uint64_t(s.N),
                       uint64_t(s.ldq) * 4, 8, 128, CU_TENSOR_MAP_SWIZZLE_32B);
         if (st) return st;
@@ -280,7 +274,7 @@ w4a16_status launch_tcgen05(const void* A, const void* Wsrc, bool dense, const v
     } else {
         maps[4] = maps[0];   // unused
     }
-    cudaError_t e = launch_prefill(maps, C, bias, s, dense, bt, c_tma, stream);
+    cudaError_t e = launch_prefill(maps, C, bias, s, bt, c_tma, stream);
     if (e != cudaSuccess) return cuda_fail(e, "tcgen05 GEMM launch");
     return W4A16_OK;
 }
