@@ -238,8 +238,8 @@ w4a16_status w4a16_dequant(const void* Wq, const void* scales, const int32_t* ze
 
 /*
  * w4a16_gemm_dense - C[M,N] = A[M,K] . W[N,K]^T on a dense dtype weight (the
- * pages' rocm_unquantized_gemm_impl on the cached copy), same tcgen05 kernel
- * as the fused path without the dequantisation stage.
+ * pages' rocm_unquantized_gemm_impl on the cached copy): a persistent tcgen05
+ * GEMM, one CTA per SM, fp32 accumulation, one RNE rounding to the dtype.
  *   A 16-byte aligned [M][K]; W 16-byte aligned [N][K]; C [M][N]; K % 16 == 0.
  */
 w4a16_status w4a16_gemm_dense(const void* A, const void* W, void* C, int64_t M, int64_t N,
