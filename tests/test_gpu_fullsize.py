@@ -128,3 +128,21 @@ def test_crossover_70b_mlp_sampled(sweep_q, ci):
     del w
     torch.cuda.empty_cache()
     assert_device_status_ok()
+
+
+# 128-token tiles with a K split over a cluster (few tiles, long K): the router's
+# choice at these shapes, checked on sampled outputs.
+@pytest.mark.parametrize("shape", [(256, 4096, 14336, 128, "uint4b8", "bf16"), (128, 4096, 8192, 64, "uint4", "fp16")],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_split_k_with_128_token_tiles_sampled(shape):
+    M, N, K, G, qt, dt = shape
+    p = synth.Problem(M, N, K, G, qt, dt, seed=3)
+    x = synth.make_inputs(p)
+    W_ref = orc.dequant(x.q, x.scales, x.zeros, G, dt)
+    rows, pairs = _sample(M, N, 8, 4096, 11)
+    ref_rows, ref_pairs = _sampled_ref(x.A, W_ref, dt, rows, pairs)
+    w = DeviceWeight(p, x.q, x.scales, x.zeros)
+    for path in ("auto", "fused_tmem"):
+        C = run_gemm(w, x.A, path=path)
+        _check_sampled(C, ref_rows, ref_pairs, rows, pairs, dt, path)
+    assert_device_status_ok()
