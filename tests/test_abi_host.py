@@ -198,3 +198,23 @@ def test_cpython_marshalling_matches_ctypes(B):
     targs[1] = object()
     with pytest.raises(AttributeError):
         B._gemm_ex_call(*targs)
+
+
+def test_out_of_range_integers_are_refused(B):
+    # a size or enum that does not fit its C parameter raises instead of being
+    # truncated to its low bits (2**32 + 128 must not pass as group size 128)
+    import ctypes
+    assert B.lib.w4a16_route(1, 4096, 4096, 128, 0, 1, 0) >= 0
+    with pytest.raises(ctypes.ArgumentError, match="OverflowError"):
+        B.lib.w4a16_route(1, 4096, 4096, 2**32 + 128, 0, 1, 0)
+    with pytest.raises(ctypes.ArgumentError, match="OverflowError"):
+        B.lib.w4a16_route(2**64 + 1, 4096, 4096, 128, 0, 1, 0)
+    base = [FAKE, FAKE, FAKE, None, None, FAKE, 4, 256, 4096, 2**32 + 128, 0, 1, 0, None]
+    with pytest.raises(ctypes.ArgumentError, match="OverflowError"):
+        B.lib.w4a16_gemm_ex(*base)
+    if B._fastcall is not None:
+        with pytest.raises(OverflowError):
+            B._gemm_ex_call(*base)
+        base[9], base[6] = 128, 2**64
+        with pytest.raises(OverflowError):
+            B._gemm_ex_call(*base)

@@ -11,6 +11,7 @@ there is no fallback.
 from __future__ import annotations
 
 import ctypes
+import operator
 import os
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -39,24 +40,46 @@ if not os.path.exists(LIB_PATH):
 
 lib = ctypes.CDLL(LIB_PATH)
 
+
+
+class _RangeCheckedInt:
+    """ctypes argument type for a C integer parameter.  ctypes itself keeps only the
+    low bits of a Python int that does not fit (2**32 + 128 would pass as 128);
+    this refuses such a value with OverflowError instead."""
+    ctype = ctypes.c_int
+    bits = 32
+
+    @classmethod
+    def from_param(cls, v):
+        v = operator.index(v)
+        if not -(1 << (cls.bits - 1)) <= v < (1 << (cls.bits - 1)):
+            raise OverflowError(f"{v} does not fit a {cls.bits}-bit C integer")
+        return cls.ctype(v)
+
+
+class _CheckedInt64(_RangeCheckedInt):
+    ctype = ctypes.c_int64
+    bits = 64
+
+
 _P = ctypes.c_void_p
-_I64 = ctypes.c_int64
-_I = ctypes.c_int
+_I64 = _CheckedInt64
+_I = _RangeCheckedInt
 _SZ = ctypes.POINTER(ctypes.c_size_t)
 
 _SIGS = {
-    "w4a16_version": (_I, []),
+    "w4a16_version": (ctypes.c_int, []),
     "w4a16_last_error_string": (ctypes.c_char_p, []),
-    "w4a16_packed_layout": (_I, [_I64, _I64, _I, _I, _I, _SZ, _SZ, _SZ, ctypes.POINTER(_I64)]),
-    "w4a16_pack": (_I, [_P, _P, _P, _P, _I64, _I64, _I, _I, _I, _P]),
-    "w4a16_pack_ex": (_I, [_P, _I, _P, _P, _I, _P, _I64, _I64, _I, _I, _I, _P]),
-    "w4a16_gemm": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _P]),
-    "w4a16_gemm_ex": (_I, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _I, _P]),
-    "w4a16_linear": (_I, [_P, _I64, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I, _I, _I, _I, _P]),
-    "w4a16_route": (_I, [_I64, _I64, _I64, _I, _I, _I, _I]),
-    "w4a16_dequant": (_I, [_P, _P, _P, _P, _I64, _I64, _I, _I, _I, _P]),
-    "w4a16_gemm_dense": (_I, [_P, _P, _P, _I64, _I64, _I64, _I, _P]),
-    "w4a16_device_status": (_I, [ctypes.POINTER(_I)]),
+    "w4a16_packed_layout": (ctypes.c_int, [_I64, _I64, _I, _I, _I, _SZ, _SZ, _SZ, ctypes.POINTER(ctypes.c_int64)]),
+    "w4a16_pack": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I, _I, _I, _P]),
+    "w4a16_pack_ex": (ctypes.c_int, [_P, _I, _P, _P, _I, _P, _I64, _I64, _I, _I, _I, _P]),
+    "w4a16_gemm": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _P]),
+    "w4a16_gemm_ex": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _I, _P]),
+    "w4a16_linear": (ctypes.c_int, [_P, _I64, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I, _I, _I, _I, _P]),
+    "w4a16_route": (ctypes.c_int, [_I64, _I64, _I64, _I, _I, _I, _I]),
+    "w4a16_dequant": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I, _I, _I, _P]),
+    "w4a16_gemm_dense": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _I64, _I, _P]),
+    "w4a16_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int)]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _f = getattr(lib, _name)

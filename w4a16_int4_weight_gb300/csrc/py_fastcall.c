@@ -11,6 +11,7 @@
  */
 #define PY_SSIZE_T_CLEAN
 #include <Python.h>
+#include <limits.h>
 #include <stdint.h>
 
 typedef int (*gemm_ex_fn)(const void* A, const void* Wq, const void* scales, const int32_t* zeros,
@@ -38,7 +39,17 @@ static void* as_ptr(PyObject* o) {
     return p;
 }
 
-static int as_int(PyObject* o) { return (int)PyLong_AsLong(o); }
+/* A Python int that fits a C int; OverflowError (set, returns 0) otherwise,
+   where a plain cast would keep only the low bits. */
+static int as_int(PyObject* o) {
+    const long v = PyLong_AsLong(o);
+    if (v == -1 && PyErr_Occurred()) return 0;
+    if (v < INT_MIN || v > INT_MAX) {
+        PyErr_Format(PyExc_OverflowError, "%ld does not fit a 32-bit C integer", v);
+        return 0;
+    }
+    return (int)v;
+}
 
 static PyObject* fc_bind(PyObject* self, PyObject* args) {
     unsigned long long gemm_ex = 0, linear = 0;
