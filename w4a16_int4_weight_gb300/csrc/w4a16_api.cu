@@ -87,6 +87,8 @@ w4a16_status check_qptrs(const void* Wq, const void* scales, const int32_t* zero
 
 // --- TMA tensor maps -------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+CtxGetCurrentFn g_ctx_get_current = nullptr;   // optional: without it, bind on every encode
 std::once_flag g_encode_once;
 cudaError_t g_encode_err = cudaSuccess;
 
@@ -100,8 +102,26 @@ w4a16_status get_encoder() {
             g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
         else if (g_encode_err == cudaSuccess)
             g_encode_err = cudaErrorSymbolNotFound;
+        fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(fn);
     });
     if (!g_encode) return cuda_fail(g_encode_err, "cuTensorMapEncodeTiled lookup");
+    return W4A16_OK;
+}
+
+// The encoder needs a current context.  A host thread whose runtime calls so
+// far made none current (cudaGetDevice does not; a launch would) has none, and
+// the encoder then fails with CUDA_ERROR_INVALID_CONTEXT.  cudaSetDevice makes
+// the device's primary context current in this thread, as a launch would.
+w4a16_status ensure_current_context() {
+    CUcontext ctx = nullptr;
+    if (g_ctx_get_current && g_ctx_get_current(&ctx) == CUDA_SUCCESS && ctx) return W4A16_OK;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaSetDevice(dev);
+    if (e != cudaSuccess) return cuda_fail(e, "making the device's primary context current");
     return W4A16_OK;
 }
 
@@ -149,6 +169,8 @@ w4a16_status make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, 
         }
     }
     w4a16_status st = get_encoder();
+    if (st) return st;
+    st = ensure_current_context();
     if (st) return st;
     cuuint64_t dims[2] = {cols, rows};
     cuuint64_t strides[1] = {row_stride_bytes};
