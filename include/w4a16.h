@@ -256,6 +256,19 @@ const char* w4a16_last_error_string(void);
  */
 w4a16_status w4a16_device_status(int* site);
 
+/*
+ * w4a16_selftest_wait_timeout - exercise the failure-detection path on the
+ * device.  Enqueues a one-warp kernel that waits, through the same bounded
+ * barrier wait every kernel of the library uses, on an mbarrier that nothing
+ * ever completes.  After the wait limit (about one second) the wait gives up,
+ * records site W4A16_SELFTEST_SITE in the library's device status word and the
+ * kernel returns: nothing faults, nothing hangs, and the device stays usable.
+ * A following w4a16_device_status() returns W4A16_ERR_DEVICE_TIMEOUT with that
+ * site (and clears it).  Returns W4A16_ERR_CUDA if the launch fails.
+ */
+#define W4A16_SELFTEST_SITE 90
+w4a16_status w4a16_selftest_wait_timeout(void* stream);
+
 /* Library version, e.g. 100 for 0.1.0. */
 int w4a16_version(void);
 

@@ -80,6 +80,7 @@ _SIGS = {
     "w4a16_dequant": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I, _I, _I, _P]),
     "w4a16_gemm_dense": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _I64, _I, _P]),
     "w4a16_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int)]),
+    "w4a16_selftest_wait_timeout": (ctypes.c_int, [_P]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _f = getattr(lib, _name)
@@ -247,3 +248,13 @@ def device_status():
     site = ctypes.c_int(0)
     code = lib.w4a16_device_status(ctypes.byref(site))
     return code, site.value
+
+
+SELFTEST_SITE = 90   # W4A16_SELFTEST_SITE
+
+
+def selftest_wait_timeout(stream=None):
+    """Enqueue the failure-detection self-test: one warp's bounded wait on a barrier
+    that nothing completes gives up after about a second; device_status() then
+    reports (ERR_DEVICE_TIMEOUT, SELFTEST_SITE)."""
+    _check(lib.w4a16_selftest_wait_timeout(_stream(stream)))

@@ -90,4 +90,9 @@ cudaError_t launch_dense_gemm(const CUtensorMap* maps, void* C, const void* bias
                               int num_sms, cudaStream_t stream);
 int take_status_dense();
 
+// selftest.cu: one warp waits on an mbarrier that nothing completes; the bounded
+// wait gives up after its limit and records `site` in this module's status word.
+cudaError_t launch_wait_timeout(int site, cudaStream_t stream);
+int take_status_selftest();
+
 }  // namespace w4a16

@@ -376,6 +376,12 @@ extern "C" {
 
 int w4a16_version(void) { return 100; }
 
+w4a16_status w4a16_selftest_wait_timeout(void* stream) {
+    cudaError_t e = launch_wait_timeout(W4A16_SELFTEST_SITE, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "self-test kernel launch");
+    return W4A16_OK;
+}
+
 const char* w4a16_last_error_string(void) { return g_err; }
 
 w4a16_status w4a16_packed_layout(int64_t N, int64_t K, int G, int qtype, int dtype,
@@ -555,6 +561,7 @@ w4a16_status w4a16_device_status(int* site) {
     if (v == 0) v = take_status_prefill();
     if (v == 0) v = take_status_tmem_gemm();
     if (v == 0) v = take_status_dense();
+    if (v == 0) v = take_status_selftest();
     if (site) *site = v > 0 ? v : 0;
     if (v < 0) return fail(W4A16_ERR_CUDA, "reading the device status word failed");
     if (v > 0) return fail(W4A16_ERR_DEVICE_TIMEOUT, "a kernel barrier wait timed out at site %d", v);
