@@ -205,6 +205,12 @@ def test_out_of_range_integers_are_refused(B):
     # truncated to its low bits (2**32 + 128 must not pass as group size 128)
     import ctypes
     assert B.lib.w4a16_route(1, 4096, 4096, 128, 0, 1, 0) >= 0
+    # ctypes integer objects and numpy integers are taken at their value
+    import numpy as np
+    assert B.lib.w4a16_route(ctypes.c_int64(1), np.int64(4096), 4096, ctypes.c_int(128), 0, 1, 0) == \
+        B.lib.w4a16_route(1, 4096, 4096, 128, 0, 1, 0)
+    with pytest.raises(ctypes.ArgumentError, match="TypeError"):
+        B.lib.w4a16_route(ctypes.c_double(1.0), 4096, 4096, 128, 0, 1, 0)
     with pytest.raises(ctypes.ArgumentError, match="OverflowError"):
         B.lib.w4a16_route(1, 4096, 4096, 2**32 + 128, 0, 1, 0)
     with pytest.raises(ctypes.ArgumentError, match="OverflowError"):

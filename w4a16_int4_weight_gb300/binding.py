@@ -51,6 +51,8 @@ class _RangeCheckedInt:
 
     @classmethod
     def from_param(cls, v):
+        if isinstance(v, ctypes._SimpleCData):   # a ctypes integer object, as ctypes accepts
+            v = v.value
         v = operator.index(v)
         if not -(1 << (cls.bits - 1)) <= v < (1 << (cls.bits - 1)):
             raise OverflowError(f"{v} does not fit a {cls.bits}-bit C integer")
