@@ -105,7 +105,12 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
                                                           const __grid_constant__ CUtensorMap tmap_z,
                                                           const Params p) {
     constexpr int MP = 8 * NT;                      // padded token count of the MMA column tiles
-    constexpr int NSETS = NT == 1 ? 2 : 1;          // independent accumulator chains per tile
+    // Independent accumulator chains per token tile.  Two chains shorten the MMA
+    // dependency chain but cost a merge per group; measured on GB300 (70B MLP and
+    // 11008x4096 layers, M = 1 and 8), one chain is faster at 32-wide groups
+    // (2.5-5 %) and for fp16 at 64-wide groups (2.6 %), two elsewhere (bf16 at
+    // G = 64: 4.6 %).
+    constexpr int NSETS = (NT == 1 && (WPG >= 4 || (BF16 && WPG == 2))) ? 2 : 1;
     constexpr int GPB = 8 / WPG;                    // groups per box (1 in the large-group mode)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
