@@ -34,6 +34,13 @@
  *     word and the kernel returns without hanging; w4a16_device_status() reads it.
  *   - dtype is the activation = scale = output type; fp16 or bf16.
  *   - Sizes are int64_t and must be < 2^31.
+ *   - Calls may come from several host threads at once (the host caches are
+ *     locked; a thread that has not used CUDA yet gets the current device's
+ *     primary context made current).  The GEMM, dequant and pack entry points
+ *     may be captured into a CUDA graph: they only launch kernels on `stream`,
+ *     whose arguments (tensor maps included) are fixed at capture.
+ *   - Results are deterministic: no kernel uses atomics to combine partial
+ *     sums, and K-split partials are added in a fixed order.
  */
 #ifndef W4A16_H_
 #define W4A16_H_
