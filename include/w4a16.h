@@ -55,7 +55,7 @@ extern "C" {
 typedef enum {
     W4A16_OK = 0,
     W4A16_ERR_INVALID_ARG = 1,     /* a shape, pointer, alignment or enum was rejected */
-    W4A16_ERR_UNSUPPORTED = 2,     /* valid arguments outside what this build implements */
+    W4A16_ERR_UNSUPPORTED = 2,     /* valid arguments outside what this library implements */
     W4A16_ERR_CUDA = 3,            /* a CUDA runtime/driver call failed (message has details) */
     W4A16_ERR_DEVICE_TIMEOUT = 4   /* a kernel's bounded barrier wait ran out */
 } w4a16_status;
