@@ -234,6 +234,30 @@ w4a16_status w4a16_linear(const void* A, int64_t lda, const void* Wq, const void
 int w4a16_route(int64_t M, int64_t N, int64_t K, int G, int qtype, int dtype, int has_dense);
 
 /*
+ * w4a16_launch_plan - how w4a16_gemm_ex / w4a16_linear would launch for these
+ * sizes on a GPU with num_sms SMs.  Host-only: touches no device.
+ *   path       W4A16_PATH_AUTO (resolved by the router, has_dense as in
+ *              w4a16_route), _FUSED, or one kernel by name.
+ *   info       receives the kernel (path, always a specific one), the tokens per
+ *              CTA tile, the CTAs per cluster that split K (1 = none), the depth
+ *              of the small-M kernel's TMA ring (0 for the other kernels), the
+ *              CTAs launched and the small-M kernel's dynamic shared memory per
+ *              CTA (0 for the other kernels).
+ * Returns W4A16_ERR_INVALID_ARG for arguments w4a16_gemm_ex would reject
+ * (pointers aside), W4A16_ERR_UNSUPPORTED where it would be unsupported.
+ */
+typedef struct {
+    int path;
+    int token_tile;
+    int k_split;
+    int stages;
+    int64_t grid;
+    int64_t smem_bytes;
+} w4a16_launch_info;
+w4a16_status w4a16_launch_plan(int64_t M, int64_t N, int64_t K, int G, int qtype, int dtype,
+                               int path, int has_dense, int num_sms, w4a16_launch_info* info);
+
+/*
  * w4a16_dequant - dense copy W[n][k] = rne_dtype((q[n][k] - zero) * scale), the
  * pages' dequantize_w4a16.  Bit-exact: (q - zero) * scale is exact in float32,
  * so the single rounding to dtype is the only one.

@@ -64,6 +64,12 @@ class _CheckedInt64(_RangeCheckedInt):
     bits = 64
 
 
+class LaunchInfo(ctypes.Structure):
+    """w4a16_launch_info."""
+    _fields_ = [("path", ctypes.c_int), ("token_tile", ctypes.c_int), ("k_split", ctypes.c_int),
+                ("stages", ctypes.c_int), ("grid", ctypes.c_int64), ("smem_bytes", ctypes.c_int64)]
+
+
 _P = ctypes.c_void_p
 _I64 = _CheckedInt64
 _I = _RangeCheckedInt
@@ -79,6 +85,7 @@ _SIGS = {
     "w4a16_gemm_ex": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _I, _P]),
     "w4a16_linear": (ctypes.c_int, [_P, _I64, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I, _I, _I, _I, _P]),
     "w4a16_route": (ctypes.c_int, [_I64, _I64, _I64, _I, _I, _I, _I]),
+    "w4a16_launch_plan": (ctypes.c_int, [_I64, _I64, _I64, _I, _I, _I, _I, _I, _I, ctypes.POINTER(LaunchInfo)]),
     "w4a16_dequant": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I, _I, _I, _P]),
     "w4a16_gemm_dense": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _I64, _I, _P]),
     "w4a16_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int)]),
@@ -260,3 +267,18 @@ def selftest_wait_timeout(stream=None):
     that nothing completes gives up after about a second; device_status() then
     reports (ERR_DEVICE_TIMEOUT, SELFTEST_SITE)."""
     _check(lib.w4a16_selftest_wait_timeout(_stream(stream)))
+
+
+PATH_NAMES = {v: k for k, v in PATHS.items()}
+
+
+def launch_plan(M, N, K, G, qtype, dtype, path="auto", has_dense=False, num_sms=152):
+    """How gemm_ex would launch on a GPU with num_sms SMs (host-only): a dict with the
+    kernel ("decode", "fused_tmem", "fused_smem" or "dense"), token_tile, k_split,
+    stages, grid and smem_bytes."""
+    p = PATHS[path] if isinstance(path, str) else int(path)
+    info = LaunchInfo()
+    _check(lib.w4a16_launch_plan(M, N, K, G, _qt(qtype), _dt(dtype), p, 1 if has_dense else 0,
+                                 num_sms, ctypes.byref(info)))
+    return {"path": PATH_NAMES[info.path], "token_tile": info.token_tile, "k_split": info.k_split,
+            "stages": info.stages, "grid": info.grid, "smem_bytes": info.smem_bytes}

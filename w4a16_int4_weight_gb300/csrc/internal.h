@@ -76,6 +76,8 @@ cudaError_t launch_prefill(const CUtensorMap* maps, void* C, const void* bias, c
 // box {16, gps}, gps = decode_scale_box_rows(g_eff, ng); maps[4]: C [M][N] box {128, BT},
 // valid when c_tma (16-byte aligned base and row pitch).
 int tmem_gemm_token_tile(int64_t M);
+// CTAs per cluster that split K (1, 2, 4 or 8) for the tensor-memory kernel.
+int tmem_gemm_ksplit(int64_t M, int64_t N, int64_t K, int num_sms);
 cudaError_t launch_tmem_gemm(const CUtensorMap* maps, void* C, const void* bias, const LayerShape& s,
                              int num_sms, bool prefetch_weights, bool c_tma, cudaStream_t stream);
 int take_status_tmem_gemm();

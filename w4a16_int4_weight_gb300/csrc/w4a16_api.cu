@@ -449,6 +449,51 @@ int w4a16_route(int64_t M, int64_t N, int64_t K, int G, int qtype, int dtype, in
     return route_impl(s, has_dense != 0);
 }
 
+w4a16_status w4a16_launch_plan(int64_t M, int64_t N, int64_t K, int G, int qtype, int dtype,
+                               int path, int has_dense, int num_sms, w4a16_launch_info* info) {
+    LayerShape s;
+    w4a16_status st = check_weight(N, K, G, qtype, dtype, &s);
+    if (st) return st;
+    if (!info) return fail(W4A16_ERR_INVALID_ARG, "info must not be NULL");
+    if (M < 1 || M > kMaxDim) return fail(W4A16_ERR_INVALID_ARG, "M=%lld out of range", (long long)M);
+    if (num_sms < 1 || num_sms > 4096) return fail(W4A16_ERR_INVALID_ARG, "num_sms=%d out of range", num_sms);
+    if (path < W4A16_PATH_AUTO || path > W4A16_PATH_FUSED_SMEM) return fail(W4A16_ERR_INVALID_ARG, "unknown path %d", path);
+    s.M = M;
+    if (path == W4A16_PATH_AUTO) path = route_impl(s, has_dense != 0);
+    if (path == W4A16_PATH_FUSED) path = fused_kernel_for(M);
+    constexpr int64_t kRows = 128;   // weight rows per CTA tile in every GEMM kernel
+    const int64_t row_tiles = (N + kRows - 1) / kRows;
+    w4a16_launch_info r = {path, 0, 1, 0, 0, 0};
+    if (path == W4A16_PATH_DECODE) {
+        if (M > kDecodeMaxM) return fail(W4A16_ERR_INVALID_ARG, "the decode path takes M <= %lld", (long long)kDecodeMaxM);
+        int ks, stages, nt;
+        size_t smem;
+        if (!plan_decode(M, N, K, s.g_eff, s.ng, s.zp, num_sms, &ks, &stages, &smem, &nt))
+            return fail(W4A16_ERR_UNSUPPORTED, "decode path: no launch plan fits for M=%lld, K=%lld", (long long)M, (long long)K);
+        r.token_tile = 8 * nt;
+        r.k_split = ks;
+        r.stages = stages;
+        r.grid = row_tiles * ks;
+        r.smem_bytes = int64_t(smem);
+    } else if (path == W4A16_PATH_FUSED_TMEM) {
+        const int bt = tmem_gemm_token_tile(M);
+        r.token_tile = bt;
+        r.k_split = tmem_gemm_ksplit(M, N, K, num_sms);
+        r.grid = row_tiles * ((M + bt - 1) / bt) * r.k_split;
+    } else if (path == W4A16_PATH_FUSED_SMEM) {
+        const int bt = token_tile_for(M);
+        r.token_tile = bt;
+        r.grid = row_tiles * ((M + bt - 1) / bt);
+    } else {   // W4A16_PATH_DENSE: persistent, one CTA per SM at most
+        const int64_t tiles = row_tiles * ((M + 255) / 256);
+        r.token_tile = 256;
+        r.grid = tiles < num_sms ? tiles : num_sms;
+    }
+    *info = r;
+    g_err[0] = '\0';
+    return W4A16_OK;
+}
+
 w4a16_status w4a16_linear(const void* A, int64_t lda, const void* Wq, const void* scales,
                           const int32_t* zeros, const void* bias, const void* Wdense, void* C,
                           int64_t ldc, int64_t M, int64_t N, int64_t K, int G, int qtype, int dtype,
