@@ -11,6 +11,7 @@ identities fixed by the pages or by mathematics.
 
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import subprocess
@@ -30,6 +31,12 @@ _lock = threading.Lock()
 _lib = None
 
 
+def _compile(src: str, out: str) -> None:
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+           "-fno-fast-math", "-ffp-contract=off", src, "-o", out, "-lm"]
+    subprocess.run(cmd, check=True)
+
+
 def build(force: bool = False) -> str:
     """Compile the oracle with gcc (-O2, OpenMP, no fast-math)."""
     os.makedirs(_BUILD_DIR, exist_ok=True)
@@ -37,52 +44,88 @@ def build(force: bool = False) -> str:
             and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
-           "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
-    subprocess.run(cmd, check=True)
+    _compile(_SRC, tmp)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
+
+
+def source() -> str:
+    """Text of the oracle's C source."""
+    with open(_SRC) as f:
+        return f.read()
+
+
+def build_variant(text: str, out_dir: str) -> str:
+    """Compile a modified copy of the C source (for tests that plant a mistake in
+    the oracle and check that a pin catches it); returns the library path."""
+    src = os.path.join(out_dir, "w4a16_oracle_variant.c")
+    with open(src, "w") as f:
+        f.write(text)
+    out = os.path.join(out_dir, "liborc_variant.so")
+    _compile(src, out)
+    return out
+
+
+def _configure(lib):
+    P = ctypes.c_void_p
+    I64 = ctypes.c_int64
+    I = ctypes.c_int
+    sig = {
+        "orc_num_threads": (I, []),
+        "orc_f16_value": (ctypes.c_double, [ctypes.c_uint16]),
+        "orc_bf16_value": (ctypes.c_double, [ctypes.c_uint16]),
+        "orc_round_f16": (ctypes.c_uint16, [ctypes.c_double]),
+        "orc_round_bf16": (ctypes.c_uint16, [ctypes.c_double]),
+        "orc_values": (None, [P, I64, I, P]),
+        "orc_round": (None, [P, I64, I, P]),
+        "orc_shift_table": (I, [I]),
+        "orc_pack_q": (None, [P, I64, I64, I64, P]),
+        "orc_unpack_q": (None, [P, I64, I64, I64, P]),
+        "orc_zero_point": (I, [P, I64, I64, I64]),
+        "orc_dequant": (None, [P, P, P, I64, I64, I64, I, P]),
+        "orc_gemm": (None, [P, P, I64, I64, I64, I, P]),
+        "orc_gemm_rows": (None, [P, P, P, I64, I64, I64, I, P]),
+        "orc_gemm_pairs": (None, [P, P, P, P, I64, I64, I, P]),
+        "orc_linear_rows": (I, [P, P, I64, P, P, P, I64, I64, I64, I64, I, P]),
+        "orc_add_bias": (None, [P, I64, I64, P, I]),
+        "orc_encode_gptq": (None, [P, I64, I64, P]),
+        "orc_decode_gptq": (None, [P, I64, I64, P]),
+        "orc_encode_kn": (None, [P, I64, I64, P]),
+        "orc_decode_kn": (None, [P, I64, I64, P]),
+        "orc_encode_exllama": (None, [P, I64, I64, P]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    return lib
 
 
 def _load():
     global _lib
     with _lock:
-        if _lib is not None:
-            return _lib
-        lib = ctypes.CDLL(build())
-        P = ctypes.c_void_p
-        I64 = ctypes.c_int64
-        I = ctypes.c_int
-        sig = {
-            "orc_num_threads": (I, []),
-            "orc_f16_value": (ctypes.c_double, [ctypes.c_uint16]),
-            "orc_bf16_value": (ctypes.c_double, [ctypes.c_uint16]),
-            "orc_round_f16": (ctypes.c_uint16, [ctypes.c_double]),
-            "orc_round_bf16": (ctypes.c_uint16, [ctypes.c_double]),
-            "orc_values": (None, [P, I64, I, P]),
-            "orc_round": (None, [P, I64, I, P]),
-            "orc_shift_table": (I, [I]),
-            "orc_pack_q": (None, [P, I64, I64, I64, P]),
-            "orc_unpack_q": (None, [P, I64, I64, I64, P]),
-            "orc_zero_point": (I, [P, I64, I64, I64]),
-            "orc_dequant": (None, [P, P, P, I64, I64, I64, I, P]),
-            "orc_gemm": (None, [P, P, I64, I64, I64, I, P]),
-            "orc_gemm_rows": (None, [P, P, P, I64, I64, I64, I, P]),
-            "orc_gemm_pairs": (None, [P, P, P, P, I64, I64, I, P]),
-            "orc_linear_rows": (I, [P, P, I64, P, P, P, I64, I64, I64, I64, I, P]),
-            "orc_add_bias": (None, [P, I64, I64, P, I]),
-            "orc_encode_gptq": (None, [P, I64, I64, P]),
-            "orc_decode_gptq": (None, [P, I64, I64, P]),
-            "orc_encode_kn": (None, [P, I64, I64, P]),
-            "orc_decode_kn": (None, [P, I64, I64, P]),
-            "orc_encode_exllama": (None, [P, I64, I64, P]),
-        }
-        for name, (res, args) in sig.items():
-            f = getattr(lib, name)
-            f.restype = res
-            f.argtypes = args
+        if _lib is None:
+            _lib = _configure(ctypes.CDLL(build()))
+        return _lib
+
+
+def load_variant(path: str):
+    """A library built by build_variant, with the oracle's signatures."""
+    return _configure(ctypes.CDLL(path))
+
+
+@contextlib.contextmanager
+def using_library(lib):
+    """Route every oracle call to `lib` (a load_variant result) inside the block."""
+    global _lib
+    prev = _load()
+    with _lock:
         _lib = lib
-        return lib
+    try:
+        yield
+    finally:
+        with _lock:
+            _lib = prev
 
 
 def _ptr(a):
