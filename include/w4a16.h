@@ -32,6 +32,9 @@
  *   - Kernels bound every wait on a barrier (about one second).  A wait that
  *     runs out records W4A16_ERR_DEVICE_TIMEOUT in the library's device status
  *     word and the kernel returns without hanging; w4a16_device_status() reads it.
+ *     The outputs such a kernel could not complete are written as NaN, but the
+ *     call that enqueued it has already returned W4A16_OK: a caller that must
+ *     not consume such results checks w4a16_device_status() after a run.
  *   - dtype is the activation = scale = output type; fp16 or bf16.
  *   - Sizes are int64_t and must be < 2^31.
  *   - Calls may come from several host threads at once (the host caches are
@@ -281,9 +284,10 @@ const char* w4a16_last_error_string(void);
 
 /*
  * w4a16_device_status - synchronise the current device, read and clear the
- * library's device status words.  Returns W4A16_OK, W4A16_ERR_DEVICE_TIMEOUT
- * (a kernel gave up waiting; *site, if non-NULL, receives the wait site id) or
- * W4A16_ERR_CUDA.
+ * library's device status words (every kernel module's word is read and
+ * cleared on each call).  Returns W4A16_OK, W4A16_ERR_DEVICE_TIMEOUT (a kernel
+ * gave up waiting; *site, if non-NULL, receives the wait site id of the first
+ * module, in library order, whose word was set) or W4A16_ERR_CUDA.
  */
 w4a16_status w4a16_device_status(int* site);
 

@@ -94,12 +94,30 @@ def test_plans_keep_the_kernel_constraints(B):
     assert n > 10000
 
 
+def test_route_does_not_depend_on_the_sm_count(B):
+    # w4a16_route takes no SM count: the path AUTO resolves to must be the same
+    # whatever SM count a launch is planned for, and the small-M plan must exist
+    # for every count whenever the router picks it
+    n = 0
+    for (N, K, G, qt), M in itertools.product(list(shapes())[::7], [1, 4, 9, 16, 17, 64]):
+        for dt in ("bf16", "fp16"):
+            want = B.route(M, N, K, G, qt, dt)
+            names = {v: k for k, v in B.PATHS.items()}
+            for sms in (1, 2, 7, 64, 132, 148, 152, 160, 1000, 4096):
+                p = B.launch_plan(M, N, K, G, qt, dt, "auto", False, sms)
+                assert p["path"] == names[want], (M, N, K, G, qt, dt, sms)
+                if p["path"] == "decode":
+                    check_decode(p, M, N, K)
+                n += 1
+    assert n > 1000
+
+
 def test_plans_of_the_measured_workloads(B):
     # the launches the ncu summaries were taken on
     p = B.launch_plan(8, 4096, 4096, 128, "uint4b8", "bf16")
     assert (p["path"], p["k_split"], p["stages"], p["grid"]) == ("decode", 8, 2, 256)
     p = B.launch_plan(1, 28672, 8192, 64, "uint4b8", "bf16")
-    assert (p["path"], p["k_split"], p["stages"], p["grid"]) == ("decode", 2, 3, 448)
+    assert (p["path"], p["k_split"], p["stages"], p["grid"]) == ("decode", 2, 4, 448)
     p = B.launch_plan(2048, 14336, 4096, 128, "uint4b8", "bf16")
     assert (p["path"], p["token_tile"], p["k_split"], p["grid"]) == ("fused_tmem", 128, 1, 1792)
     p = B.launch_plan(2048, 14336, 4096, 128, "uint4b8", "bf16", has_dense=True)

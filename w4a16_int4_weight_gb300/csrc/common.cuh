@@ -80,6 +80,20 @@ __device__ __forceinline__ void named_barrier_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// The same barrier, returning whether `pred` was true in any participating thread.
+__device__ __forceinline__ bool named_barrier_or(int id, int threads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(uint32_t(pred)), "r"(id), "r"(threads)
+        : "memory");
+    return r != 0;
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
                  "r"(bytes)
@@ -103,18 +117,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait for phase `parity` of `bar` to complete.  Returns false (after writing
-// `site` into *status) if it did not within kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status, int site) {
+// `site` into *status) if it did not within `limit_ns` of global time.
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t* bar, uint32_t parity, int* status, int site,
+                                                uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     uint32_t it = 0;
     while (!mbar_try_wait(bar, parity)) {
-        if ((++it & 63u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) {
+        if ((++it & 63u) == 0 && global_timer_ns() - t0 > limit_ns) {
             atomicCAS(status, 0, site);
             return false;
         }
     }
     return true;
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status, int site) {
+    return mbar_wait_limit(bar, parity, status, site, kWaitLimitNs);
 }
 
 // ---------------------------------------------------------------------------
@@ -358,6 +377,13 @@ __device__ __forceinline__ float to_f32(uint16_t bits) {
     } else {
         return __half2float(__ushort_as_half(bits));
     }
+}
+
+// Quiet NaN of the dtype: the value of outputs that a failed (timed-out) wait
+// left incomplete.
+template <bool BF16>
+__device__ __forceinline__ uint16_t nan_bits() {
+    return BF16 ? uint16_t(0x7FC0) : uint16_t(0x7E00);
 }
 
 template <bool BF16>

@@ -11,8 +11,13 @@ namespace {
 
 __device__ int g_status;
 
-// Activation box slot: 8 * NT token rows of 256 values.
-int a_slot_for(int64_t M) { return 4096 * (M <= 8 ? 1 : M <= 16 ? 2 : M <= 32 ? 4 : 8); }
+// Activation box slot: M token rows of 256 values (512 bytes each), in 1024-byte
+// units so that the scales behind it stay 128-byte aligned for TMA.
+int a_slot_for(int64_t M) { return int((M * 512 + 1023) / 1024 * 1024); }
+
+// Token columns of the split-K reduction buffer: M rounded up to even (partials
+// travel as pairs of token columns).
+int red_cols_for(int64_t M) { return int((M + 1) / 2 * 2); }
 
 int stage_bytes_for(int64_t M, int gps, bool zp) {
     using namespace decode;
@@ -74,7 +79,7 @@ bool plan_decode(int64_t M, int64_t N, int64_t K, int64_t g_eff, int64_t ng, boo
         const int64_t ctas = row_tiles * ks;
         const int64_t per = (ctas + num_sms - 1) / num_sms;
         const int64_t bp = (nboxes + ks - 1) / ks;
-        const size_t red = ks > 1 ? size_t(kBN) * 8 * nt * 4 : 0;
+        const size_t red = ks > 1 ? size_t(kBN) * red_cols_for(M) * 4 : 0;
         for (int st = 1; st <= kMaxPlanStages; ++st) {
             if (st > bp && st > 1) break;
             const size_t smem = size_t(st) * sb + kBarBytes + red + 1024;
@@ -113,6 +118,12 @@ bool plan_decode(int64_t M, int64_t N, int64_t K, int64_t g_eff, int64_t ng, boo
     return true;
 }
 
+bool decode_plan_exists(int64_t M, int64_t N, int64_t K, int64_t g_eff, int64_t ng, bool zp) {
+    int ks, stages, nt;
+    size_t smem;
+    return plan_decode(M, N, K, g_eff, ng, zp, 1, &ks, &stages, &smem, &nt);
+}
+
 cudaError_t launch_decode(const CUtensorMap* maps, void* C, const void* bias, const LayerShape& s,
                           int num_sms, bool prefetch_weights, cudaStream_t stream) {
     using namespace decode;
@@ -136,6 +147,7 @@ cudaError_t launch_decode(const CUtensorMap* maps, void* C, const void* bias, co
     p.gps = decode_scale_box_rows(s.g_eff, s.ng);
     if (p.gps < 1 || p.gps > kMaxGps) return cudaErrorInvalidValue;   // never expected
     p.a_slot = a_slot_for(s.M);
+    p.mpr = red_cols_for(s.M);
     p.stage_bytes = stage_bytes_for(s.M, p.gps, s.zp);
     p.red_off = stages * p.stage_bytes + kBarBytes;
     p.prefetch_weights = prefetch_weights ? 1 : 0;

@@ -47,6 +47,10 @@ constexpr int kWBytes = kBN * 128;       // 16 KB packed weight box
 constexpr int kMaxStages = 8;
 constexpr int kMaxGps = 8;               // groups per box at G = 32
 constexpr int kBarBytes = 256;           // mbarriers: full[kMaxStages], empty[kMaxStages], red
+// The owner of split-K rows waits for its peers' partials longer than any
+// other wait: a peer sends even after one of its own waits gave up, which can
+// happen one wait limit after the owner reached this point.
+constexpr uint64_t kReductionWaitLimitNs = 3 * kWaitLimitNs;
 
 struct Params {
     uint16_t* C;
@@ -58,7 +62,8 @@ struct Params {
     int ks;           // CTAs per cluster (K split)
     int stages;       // ring depth (<= kMaxStages)
     int gps;          // scale-tile rows per box
-    int a_slot;       // bytes of the activation box slot: [8 * NT rows][256 values] = 4096 * NT
+    int a_slot;       // bytes of the activation box slot: [M rows][256 values], 1024-byte units
+    int mpr;          // token columns of the reduction buffer: M rounded up to even
     int stage_bytes;  // bytes per stage (multiple of 1024): weights, activations, gps scale
                       // rows of 256 bytes and, with zero points, gps rows of 64 bytes
     int red_off;      // byte offset of the cluster reduction buffer
@@ -118,7 +123,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.stages * p.stage_bytes);
     uint64_t* empty = full + kMaxStages;
     uint64_t* red_bar = empty + kMaxStages;   // split K: the partials pushed into this CTA
-    float* red = reinterpret_cast<float*>(smem + p.red_off);   // [ks][kBN/ks][MP]
+    float* red = reinterpret_cast<float*>(smem + p.red_off);   // [ks][kBN/ks][mpr]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int rank = int(blockIdx.x) % p.ks;   // rank inside the cluster (cluster = (ks,1,1))
@@ -141,11 +146,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
         // The peers' partials for this CTA's rows: kBN rows x (pairs of token
         // columns below M) x 8 bytes, whatever the split.  Peers store only after
         // the cluster barrier, i.e. after every CTA has initialised red_bar.
-        if (tid == 0) {
-            int pairs = 0;
-            for (int j = 0; j < NT; ++j) pairs += min(4, max(0, (p.M - 8 * j + 1) / 2));
-            mbar_arrive_expect_tx(red_bar, uint32_t(kBN * 8 * pairs));
-        }
+        if (tid == 0) mbar_arrive_expect_tx(red_bar, uint32_t(kBN * 4 * p.mpr));
         cluster_arrive_relaxed();
     }
 
@@ -330,8 +331,10 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     const bool consumer = warp < kConsumerWarps;
     // the bias of an output row, 0 without one
     auto bias_of = [&](int n) { return p.bias && n < p.N ? to_f32<BF16>(p.bias[n]) : 0.f; };
+    // A failed wait leaves the result incomplete: those outputs become NaN.
+    const uint16_t nan_out = nan_bits<BF16>();
     if (p.ks == 1) {
-        if (consumer && !failed) {
+        if (consumer) {
             const float b0 = bias_of(n0 + r0), b1 = bias_of(n0 + r1);
 #pragma unroll
             for (int j = 0; j < NT; ++j) {
@@ -340,7 +343,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
                     const int tok = 8 * j + 2 * t + (e & 1);
                     const int n = n0 + (e < 2 ? r0 : r1);
                     if (tok < p.M && n < p.N)
-                        p.C[size_t(tok) * p.ldc + n] = from_f32<BF16>(acc[j][e] + (e < 2 ? b0 : b1));
+                        p.C[size_t(tok) * p.ldc + n] =
+                            failed ? nan_out : from_f32<BF16>(acc[j][e] + (e < 2 ? b0 : b1));
                 }
             }
         }
@@ -363,22 +367,22 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
                 if (tok >= p.M) continue;   // columns past M are never summed
                 const int row = h == 0 ? r0 : r1;
                 const int owner = row / rows_per;
-                const uint32_t off = uint32_t(((rank * rows_per + (row - owner * rows_per)) * MP + tok) * 4);
+                const uint32_t off = uint32_t(((rank * rows_per + (row - owner * rows_per)) * p.mpr + tok) * 4);
                 st_async_f32x2(cluster_map(red_s + off, uint32_t(owner)), acc[j][2 * h], acc[j][2 * h + 1],
                                cluster_map(bar_s, uint32_t(owner)));
             }
         }
     }
     // Once red_bar completes no peer writes here any more, so the CTA may retire.
-    const bool got = mbar_wait(red_bar, 0u, p.status, 4);
+    const bool got = mbar_wait_limit(red_bar, 0u, p.status, 4, kReductionWaitLimitNs);
     const int any_failed = __syncthreads_or(failed || !got);
     const int items = rows_per * p.M;
     for (int it = tid; it < items; it += kThreads) {
         const int rl = it % rows_per, tok = it / rows_per;
         float sum = 0.f;
-        for (int c = 0; c < p.ks; ++c) sum += red[(c * rows_per + rl) * MP + tok];
+        for (int c = 0; c < p.ks; ++c) sum += red[(c * rows_per + rl) * p.mpr + tok];
         const int n = n0 + rank * rows_per + rl;
-        if (n < p.N && !any_failed) p.C[size_t(tok) * p.ldc + n] = from_f32<BF16>(sum + bias_of(n));
+        if (n < p.N) p.C[size_t(tok) * p.ldc + n] = any_failed ? nan_out : from_f32<BF16>(sum + bias_of(n));
     }
 }
 

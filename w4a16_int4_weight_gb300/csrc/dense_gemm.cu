@@ -144,14 +144,21 @@ __global__ void __launch_bounds__(kThreads, 1) dense_gemm_kernel(const __grid_co
         const uint32_t lane_base = uint32_t(32 * (warp & 3)) << 16;
         const int rl = 32 * (warp & 3) + lane;
         int i = 0;
+        bool dead = false;   // a wait timed out: this and every later tile of the CTA become NaN
         for (int t = blockIdx.x; t < p.tiles; t += gridDim.x, ++i) {
             const int a = i & 1;
-            const bool ok = __all_sync(0xffffffffu, mbar_wait(&acc_full[a], uint32_t(i / 2) & 1u, status, 54));
-            if (!ok) break;   // the issuer stopped: no later tile completes either
-            tc_fence_after();
             const int n = (t / p.tiles_m) * kBM + rl;
             const int m0 = (t % p.tiles_m) * kBT;
             const bool row_ok = n < p.N;
+            if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(&acc_full[a], uint32_t(i / 2) & 1u, status, 54));
+            if (dead) {   // no tensor-memory reads: the issuer has stopped or is late
+                if (row_ok) {
+                    for (int c = (warp >> 2) * (kBT / 2); c < ((warp >> 2) + 1) * (kBT / 2); ++c)
+                        if (m0 + c < p.M) p.C[size_t(m0 + c) * p.ldc + n] = nan_bits<BF16>();
+                }
+                continue;
+            }
+            tc_fence_after();
             const float b = p.bias && row_ok ? to_f32<BF16>(p.bias[n]) : 0.f;
 #pragma unroll 1
             for (int c = (warp >> 2) * (kBT / 64); c < ((warp >> 2) + 1) * (kBT / 64); ++c) {

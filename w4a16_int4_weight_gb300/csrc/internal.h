@@ -63,6 +63,8 @@ cudaError_t launch_decode(const CUtensorMap* maps, void* C, const void* bias, co
 int decode_scale_box_rows(int64_t g_eff, int64_t ng);
 bool plan_decode(int64_t M, int64_t N, int64_t K, int64_t g_eff, int64_t ng, bool zp,
                  int num_sms, int* ks_out, int* stages_out, size_t* smem_out, int* nt_out);
+// Whether any plan fits the shape (independent of the SM count).
+bool decode_plan_exists(int64_t M, int64_t N, int64_t K, int64_t g_eff, int64_t ng, bool zp);
 
 // prefill.cu: fused-dequant tcgen05 GEMM with the dequantised tile in shared memory.
 // maps: A [M][K] box {64,BT} SW128; packed [N][ldq] box {8,128} SW32; scales [ng][lds]

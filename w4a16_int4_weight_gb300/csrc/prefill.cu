@@ -205,13 +205,25 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         if (ok) ok = mbar_wait(acc_full, 0u, p_status(), 15);
         ok = __all_sync(0xffffffffu, ok);   // tcgen05.ld below is warp-collective
         tc_fence_after();
-        if (p.c_tma) {
+        // A failed wait leaves the tile incomplete: its outputs become NaN, written
+        // directly (shared memory may still receive copies that were in flight).
+        auto nan_tile = [&]() {
+            const int n_out = n0 + 32 * (warp & 3) + lane;
+            if (n_out >= p.N) return;
+            for (int c = (warp >> 2) * (BT / 2); c < ((warp >> 2) + 1) * (BT / 2); ++c) {
+                const int tok = m0 + c;
+                if (tok < p.M) p.C[size_t(tok) * p.ldc + n_out] = nan_bits<BF16>();
+            }
+        };
+        if (p.c_tma && named_barrier_or(1, kDqWarps * 32, !ok)) {
+            nan_tile();
+        } else if (p.c_tma) {
             // Stage the output tile [BT tokens][128 rows] in the dtype in the operand
             // ring (the tensor core's reads of it completed before acc_full), then one
             // TMA store that clips rows >= N and tokens >= M.
             static_assert(kStages * L::kStageBytes >= BT * kBM * 2, "output tile fits the operand ring");
             uint16_t* stg = reinterpret_cast<uint16_t*>(smem);
-            if (ok) {
+            {
                 const uint32_t lane_base = uint32_t(32 * (warp & 3)) << 16;
                 const int rl = 32 * (warp & 3) + lane;
                 const int n_out = n0 + rl;
@@ -228,12 +240,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 fence_proxy_async_smem();
             }
             named_barrier_sync(1, kDqWarps * 32);
-            if (warp == 0 && lane == 0 && ok) {
+            if (warp == 0 && lane == 0) {
                 tma_store_2d(&tmap_c, stg, n0, m0);
                 bulk_commit_group();
                 bulk_wait_read_all();   // the tile must stay until the store has read it
             }
-        } else if (ok) {
+        } else if (!ok) {
+            nan_tile();
+        } else {
             // warp w reads TMEM lanes 32*(w%4).. (its rows) and half w/4 of the columns
             const uint32_t lane_base = uint32_t(32 * (warp & 3)) << 16;
             const int n_out = n0 + 32 * (warp & 3) + lane;

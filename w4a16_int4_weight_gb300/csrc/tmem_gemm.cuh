@@ -435,6 +435,16 @@ __global__ void __launch_bounds__(kThreads, 2) tmem_gemm_kernel(const __grid_con
     const int c0 = (warp >> 2) * kColsPerWarp;
     // the bias of an output row, 0 without one
     auto bias_of = [&](int n) { return p.bias && n < p.N ? to_f32<BF16>(p.bias[n]) : 0.f; };
+    // A failed wait leaves the tile incomplete: its outputs become NaN, written
+    // directly (shared memory may still receive copies that were in flight).
+    auto nan_tile = [&]() {
+        const int n = n0 + row;
+        if (n >= p.N) return;
+        for (int c = 0; c < kColsPerWarp; ++c) {
+            const int tok = m0 + c0 + c;
+            if (tok < p.M) p.C[size_t(tok) * p.ldc + n] = nan_bits<BF16>();
+        }
+    };
     if (p.ks == 1 && p.c_tma) {
         // Stage the output tile [BT tokens][128 rows] in the dtype in the activation
         // ring (the tensor core's last reads of it completed before acc_full), then
@@ -442,8 +452,10 @@ __global__ void __launch_bounds__(kThreads, 2) tmem_gemm_kernel(const __grid_con
         // 32 lanes straight to global memory took ~2 us of a 27 us tile.
         static_assert(L::kAUnits * L::kAUnitBytes >= BT * kBM * 2, "output tile fits the activation ring");
         uint16_t* stg = reinterpret_cast<uint16_t*>(smem + L::kActOff);
-        if (epi) {
-            if (ok && nkb > 0) {
+        if (epi && named_barrier_or(1, 4 * kHalves * 32, !(ok && nkb > 0))) {
+            nan_tile();
+        } else if (epi) {
+            {
                 const float b = bias_of(n0 + row);
 #pragma unroll 1
                 for (int c = 0; c < kColsPerWarp; c += 16) {
@@ -457,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 2) tmem_gemm_kernel(const __grid_con
                 fence_proxy_async_smem();
             }
             named_barrier_sync(1, 4 * kHalves * 32);
-            if (warp == 0 && lane == 0 && ok && nkb > 0) {
+            if (warp == 0 && lane == 0) {
                 tma_store_2d(&tmap_c, stg, n0, m0);
                 bulk_commit_group();
                 bulk_wait_read_all();   // the tile must stay until the store has read it
@@ -469,7 +481,9 @@ __global__ void __launch_bounds__(kThreads, 2) tmem_gemm_kernel(const __grid_con
         return;
     }
     if (p.ks == 1) {
-        if (epi && ok && nkb > 0) {
+        if (epi && !(ok && nkb > 0)) {
+            nan_tile();
+        } else if (epi) {
             const int n = n0 + row;
             const float b = bias_of(n);
 #pragma unroll 1
@@ -517,7 +531,9 @@ __global__ void __launch_bounds__(kThreads, 2) tmem_gemm_kernel(const __grid_con
         }
     }
     // Once red_bar completes no peer writes here any more, so the CTA may retire.
-    const bool got = mbar_wait(red_bar, 0u, p.status, 38);
+    // (the peers' sends can follow one of their own timed-out waits, so this wait
+    // is longer than any other)
+    const bool got = mbar_wait_limit(red_bar, 0u, p.status, 38, 3 * kWaitLimitNs);
     const int any_failed = __syncthreads_or(!ok || !got);
     // this CTA owns rows [rank*rows_per, (rank+1)*rows_per) of the tile
     const int items = rows_per * BT;
@@ -526,7 +542,8 @@ __global__ void __launch_bounds__(kThreads, 2) tmem_gemm_kernel(const __grid_con
         float sum = 0.f;
         for (int c = 0; c < p.ks; ++c) sum += red[(size_t(c) * rows_per + rl) * BT + col];
         const int n = n0 + rank * rows_per + rl, tok = m0 + col;
-        if (n < p.N && tok < p.M && !any_failed) p.C[size_t(tok) * p.ldc + n] = from_f32<BF16>(sum + bias_of(n));
+        if (n < p.N && tok < p.M)
+            p.C[size_t(tok) * p.ldc + n] = any_failed ? nan_bits<BF16>() : from_f32<BF16>(sum + bias_of(n));
     }
     tc_fence_before();
     __syncthreads();

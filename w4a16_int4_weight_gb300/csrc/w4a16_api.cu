@@ -225,18 +225,17 @@ constexpr int64_t kDenseFromM = 2048;
 
 int fused_kernel_for(int64_t) { return W4A16_PATH_FUSED_TMEM; }
 
+// The route depends on the shape only: whether a small-M launch plan exists
+// (its shared memory fits) does not depend on the SM count, which only changes
+// the plan's K split and ring depth, chosen at launch from the live count.
 int route_impl(const LayerShape& s, bool has_dense) {
     const int64_t M = s.M;
     // From 9 tokens (two MMA column tiles) the small-M kernel's per-group rescale
     // at G = 32 costs more than the fused kernel's dequantisation (measured:
     // 18.9 vs 15.5 us on 11008x4096; G >= 64 keeps decode ahead or level).
     const bool small_groups = s.ng > 1 && s.g_eff <= 32;
-    if (M <= kDecodeUpToM && !(M > 8 && small_groups)) {
-        int ks, stages, nt;
-        size_t smem;
-        if (plan_decode(M, s.N, s.K, s.g_eff, s.ng, s.zp, 152, &ks, &stages, &smem, &nt))
-            return W4A16_PATH_DECODE;
-    }
+    if (M <= kDecodeUpToM && !(M > 8 && small_groups) && decode_plan_exists(M, s.N, s.K, s.g_eff, s.ng, s.zp))
+        return W4A16_PATH_DECODE;
     if (has_dense && M >= kDenseFromM) return W4A16_PATH_DENSE;
     return fused_kernel_for(M);
 }
@@ -524,10 +523,8 @@ w4a16_status w4a16_linear(const void* A, int64_t lda, const void* Wq, const void
     if (path == W4A16_PATH_FUSED) path = fused_kernel_for(M);
     if (path == W4A16_PATH_DENSE && !Wdense) return fail(W4A16_ERR_INVALID_ARG, "the dense path needs a dense copy (Wdense)");
     if (path == W4A16_PATH_DECODE) {
-        int ks, stages, nt;
-        size_t smem;
         if (M > kDecodeMaxM) return fail(W4A16_ERR_INVALID_ARG, "the decode path takes M <= %lld", (long long)kDecodeMaxM);
-        if (M > 0 && !plan_decode(M, N, K, s.g_eff, s.ng, s.zp, 152, &ks, &stages, &smem, &nt))
+        if (M > 0 && !decode_plan_exists(M, N, K, s.g_eff, s.ng, s.zp))
             return fail(W4A16_ERR_UNSUPPORTED, "decode path: the activation slice for M=%lld, K=%lld does not fit in shared memory", (long long)M, (long long)K);
     }
     g_err[0] = '\0';
@@ -602,11 +599,17 @@ w4a16_status w4a16_gemm_dense(const void* A, const void* W, void* C, int64_t M, 
 w4a16_status w4a16_device_status(int* site) {
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
-    int v = take_status_decode();
-    if (v == 0) v = take_status_prefill();
-    if (v == 0) v = take_status_tmem_gemm();
-    if (v == 0) v = take_status_dense();
-    if (v == 0) v = take_status_selftest();
+    // read and clear every module's word, then report the first set one
+    const int words[5] = {take_status_decode(), take_status_prefill(), take_status_tmem_gemm(),
+                          take_status_dense(), take_status_selftest()};
+    int v = 0;
+    for (int w : words) {
+        if (w < 0) {
+            v = -1;
+            break;
+        }
+        if (v == 0 && w > 0) v = w;
+    }
     if (site) *site = v > 0 ? v : 0;
     if (v < 0) return fail(W4A16_ERR_CUDA, "reading the device status word failed");
     if (v > 0) return fail(W4A16_ERR_DEVICE_TIMEOUT, "a kernel barrier wait timed out at site %d", v);
