@@ -1,18 +1,19 @@
 #!/usr/bin/env python
 """Benchmark of the W4A16 int4-weight linear layer on GB300.
 
-Default workload: decode GEMV on a 7B attention-projection shape,
-M in {1, 4, 8}, K = N = 4096, group size 128, uint4b8, bf16 activations,
-seeded synthetic weights and activations.  One step runs the layer for each of
-the three M values on each of L = 32 distinct weight copies (32 x 8.65 MB =
-277 MB > the 129 MB L2), so every step streams its weights from HBM, like a
-decode pass over a stack of layers.
+Default workload: the 70B-MLP layer (K = 8192, N = 28672), group size 64,
+uint4b8, bf16 activations, seeded synthetic weights and activations.  One step
+runs the layer at every decode batch size M in {1, 2, 4, 8, 16} on each of two
+distinct weight copies (2 x 125 MB > the 129 MB L2), so every launch streams
+its weights from HBM.  `per_m` times the same layer at every M of the
+crossover sweep (1 .. 4096) through the router: HBM-bound decode at small M,
+tensor-bound prefill at large M.
 
 Prints one JSON line (rank 0).  `value` is whole-job weight throughput
-(packed q + scale bytes per second) with inputs resident in HBM, from CUDA
-events around K replays of a CUDA graph of one step; `e2e` is the same metric
-through the C ABI called eagerly with the activations copied from pinned host
-memory and the outputs copied back inside the timed region.
+(packed q + scale bytes per second) of the decode points with inputs resident
+in HBM, from CUDA events around K replays of a CUDA graph of one step; `e2e` is
+the same metric through the C ABI called eagerly with the activations copied
+from pinned host memory and the outputs copied back inside the timed region.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -41,11 +42,12 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "W4A16 GEMM TFLOP/s and weight GB/s vs M; % of HBM / bf16 tensor roofline"
-WORKLOAD = "decode_gemv_k4096_n4096_g128_uint4b8_bf16_m1_4_8"
-MS = (1, 4, 8)
-N_, K_, G_ = 4096, 4096, 128
+WORKLOAD = "mlp70b_k8192_n28672_g64_uint4b8_bf16_decode_m1_2_4_8_16"
+MS = (1, 2, 4, 8, 16)                      # the decode points of one step
+PER_M = (1, 2, 4, 8, 16, 32, 64, 128, 256, 512, 1024, 4096)   # the "vs M" curve
+N_, K_, G_ = 28672, 8192, 64
 QTYPE, DTYPE = "uint4b8", "bf16"
-LAYERS = 32
+LAYERS = 2                                 # distinct weight copies: 2 x 125 MB > L2
 L2_BYTES = 129 * 1024 * 1024
 
 
@@ -61,7 +63,7 @@ def alg_bytes(M, N, K, G, zp):
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true", help="skip the prefill/zero-point side measurements")
@@ -205,15 +207,31 @@ def measured_peaks():
 # ---------------------------------------------------------------------------
 # CPU oracle timing (cpu_baseline / reference arm)
 # ---------------------------------------------------------------------------
+def cpu_model():
+    """The host CPU's model name (lscpu), for the baseline's record."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
 _ORACLE_INPUTS = {}
+ORACLE_COLS = 2048   # output columns the oracle inputs are generated for
 
 
 def oracle_inputs(layer):
-    """Seeded inputs of one layer (generated once, outside any timed region)."""
+    """Seeded inputs of the first ORACLE_COLS output columns of one layer of the
+    workload (the generators are counter-based, so these are exactly the first
+    rows of the full weight), generated once, outside any timed region."""
     if layer not in _ORACLE_INPUTS:
         import oracle as orc
         from w4a16_int4_weight_gb300 import inputs as synth
-        p = synth.Problem(max(MS), N_, K_, G_, QTYPE, DTYPE, seed=layer)
+        p = synth.Problem(max(MS), ORACLE_COLS, K_, G_, QTYPE, DTYPE, seed=layer)
         q, s, _ = synth.make_weights(p)
         _ORACLE_INPUTS[layer] = (orc.pack_q(q), s, synth.make_activations(p))
     return _ORACLE_INPUTS[layer]
@@ -221,7 +239,7 @@ def oracle_inputs(layer):
 
 def oracle_sample(n_cols, layer=0):
     """Time the oracle on the first n_cols output columns of one layer, for each
-    of the three M.  Returns (seconds, weight bytes processed)."""
+    decode M of the step.  Returns (seconds, weight bytes processed)."""
     import oracle as orc
     words, s, A = oracle_inputs(layer)
     rows = np.arange(max(MS))
@@ -240,9 +258,9 @@ def run_reference(args, world, rank):
     import oracle as orc
     orc.build()
     # size each step so that warmup + steps stay within about two minutes
-    t, b = oracle_sample(256)
+    t, b = oracle_sample(64)
     per_step_budget = 100.0 / max(1, args.steps + args.warmup)
-    n_cols = int(max(8, min(N_, 256 * per_step_budget / max(t, 1e-6))) // 8 * 8)
+    n_cols = int(max(8, min(ORACLE_COLS, 64 * per_step_budget / max(t, 1e-6))) // 8 * 8)
     for _ in range(args.warmup):
         oracle_sample(n_cols)
     tt, bb = 0.0, 0
@@ -252,7 +270,7 @@ def run_reference(args, world, rank):
         bb += b
     value = bb / tt / 1e9
     sample = (f"oracle (unpack -> dequant -> float64 GEMM) on output columns 0..{n_cols - 1} of one "
-              f"layer for M = 1, 4, 8 per step")
+              f"layer for M = {', '.join(map(str, MS))} per step")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tt / args.steps,
@@ -261,7 +279,7 @@ def run_reference(args, world, rank):
         "config": {"workload": WORKLOAD, "M": list(MS), "K": K_, "N": N_, "group_size": G_,
                    "qtype": QTYPE, "act_dtype": DTYPE},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": orc.num_threads(), "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "cpu_model": cpu_model()},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -308,11 +326,29 @@ def time_graph(torch, fn, reps, warmup):
 
 
 def extras(torch, B, synth, peaks):
-    """Side measurements on the other workloads (not the headline): the prefill
-    tcgen05 kernel (fused and dense) and the zero-point decode pair."""
+    """Side measurements on the other workloads (not the headline): the decode
+    GEMV on the 7B attention shape, the prefill tcgen05 kernels (fused and
+    dense), the dequant kernel and the zero-point decode pair."""
     hbm, tc_burst, _, kind = peaks
     out = {}
     tdt = torch.bfloat16
+    # decode GEMV, K = N = 4096, G = 128, uint4b8, M = 1, 4, 8: 32 weight copies
+    # (277 MB > L2), each M a CUDA graph of the 32 layers
+    N, K, G, L = 4096, 4096, 128, 32
+    lay = make_layers(torch, B, synth, L, 8, N, K, G, "uint4b8", "bf16", seed0=300)
+    A = torch.randn(8, K, device="cuda").to(tdt)
+    Cs = torch.empty(L, 8, N, dtype=tdt, device="cuda")
+    for M in (1, 4, 8):
+        def run_g(M=M):
+            for l, (_, wq, sp, _) in enumerate(lay):
+                B.gemm_ex(A, wq, sp, None, None, Cs[l], M, N, K, G, "uint4b8", "bf16", "auto",
+                          static_weights=True)
+        t = time_graph(torch, run_g, 300, 10) / L
+        byts = alg_bytes(M, N, K, G, False)
+        out[f"decode_m{M}_k4096_n4096_g128"] = {"us": t * 1e6, "gbs": byts / t / 1e9,
+                                               "frac_of_hbm": byts / t / 1e9 / hbm}
+    del lay, Cs
+    torch.cuda.empty_cache()
     # prefill M=2048, K=4096, N=14336, G=128, uint4b8: 4 weight copies rotate
     M, N, K, G = 2048, 14336, 4096, 128
     lay = make_layers(torch, B, synth, 4, M, N, K, G, "uint4b8", "bf16", seed0=100)
@@ -493,19 +529,22 @@ def main():
     peaks = measured_peaks()
     hbm_peak, tc_peak, _, peak_kind = peaks
     tdt = torch.bfloat16
-    layers = make_layers(torch, B, synth, LAYERS, max(MS), N_, K_, G_, QTYPE, DTYPE)
-    A_host = {M: torch.from_numpy(synth.make_activations(synth.Problem(M, N_, K_, G_, QTYPE, DTYPE, seed=7)).view(np.int16)).view(tdt) for M in MS}
-    A_dev = {M: A_host[M].cuda() for M in MS}
+    mmax = max(PER_M)
+    layers = make_layers(torch, B, synth, LAYERS, 1, N_, K_, G_, QTYPE, DTYPE)
+    A_host = torch.from_numpy(synth.make_activations(
+        synth.Problem(mmax, N_, K_, G_, QTYPE, DTYPE, seed=7)).view(np.int16)).view(tdt)
+    A_dev = A_host.cuda()
     C_dev = {M: torch.empty(LAYERS, M, N_, dtype=tdt, device="cuda") for M in MS}
+    C_big = torch.empty(LAYERS, mmax, N_, dtype=tdt, device="cuda")
 
     # the packed weights are written once before timing and then only read, so
     # the layer is called with the static-weights promise (W4A16_OPT_STATIC_WEIGHTS);
     # each layer's output view is made once, as a serving loop holds its buffers
     C_view = {M: [C_dev[M][l] for l in range(LAYERS)] for M in MS}
 
-    def gemm(M, l, wq, sp):
-        B.gemm_ex(A_dev[M], wq, sp, None, None, C_view[M][l], M, N_, K_, G_, QTYPE, DTYPE, "auto",
-                  static_weights=True)
+    def gemm(M, l, wq, sp, C=None):
+        B.gemm_ex(A_dev, wq, sp, None, None, C_view[M][l] if C is None else C, M, N_, K_, G_, QTYPE,
+                  DTYPE, "auto", static_weights=True)
 
     def step():
         for M in MS:
@@ -545,18 +584,24 @@ def main():
     ms_per_step = 1e3 * t_max / args.steps
     value = world * args.steps * wbytes_step / t_max / 1e9
 
-    # per-M breakdown (graph of the 32 layers at one M)
+    # ---- the "vs M" curve: every M of the sweep through the router ----
+    names = {v: k for k, v in B.PATHS.items()}
     per_m = {}
-    for M in MS:
+    for M in PER_M:
         def one_m(M=M):
             for l, (_, wq, sp, _) in enumerate(layers):
-                gemm(M, l, wq, sp)
-        t = time_graph(torch, one_m, 300, 10) / LAYERS
-        per_m[str(M)] = {"us_per_launch": t * 1e6,
+                gemm(M, l, wq, sp, C_big[l] if M not in C_view else None)
+        reps = 200 if M <= 64 else 30 if M <= 512 else 5
+        t = time_graph(torch, one_m, reps, 3) / LAYERS
+        ab = alg_bytes(M, N_, K_, G_, False)
+        fl = 2.0 * M * N_ * K_
+        t_star = max(ab / (hbm_peak * 1e9), fl / (tc_peak * 1e12))
+        per_m[str(M)] = {"path": names.get(B.route(M, N_, K_, G_, QTYPE, DTYPE), "?"),
+                         "us_per_launch": t * 1e6,
                          "weight_gbs": weight_bytes(N_, K_, G_, False) / t / 1e9,
-                         "alg_gbs": alg_bytes(M, N_, K_, G_, False) / t / 1e9,
-                         "tflops": 2.0 * M * N_ * K_ / t / 1e12,
-                         "frac_of_hbm": alg_bytes(M, N_, K_, G_, False) / t / 1e9 / hbm_peak}
+                         "alg_gbs": ab / t / 1e9, "tflops": fl / t / 1e12,
+                         "frac_of_hbm": ab / t / 1e9 / hbm_peak,
+                         "frac_of_bf16": fl / t / 1e12 / tc_peak, "t_star_over_t": t_star / t}
 
     # spread of single steps: 200 graph replays, each between its own events
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(200)]
@@ -569,28 +614,20 @@ def main():
     step_spread = {"steps": len(step_ms), "p10_ms": step_ms[len(step_ms) // 10],
                    "p50_ms": step_ms[len(step_ms) // 2], "p90_ms": step_ms[(9 * len(step_ms)) // 10]}
 
-    # hot L2: one layer's weights (8.4 MB, resident in L2) called LAYERS times per M
-    hot_l2 = {}
-    for M in MS:
-        def hot_m(M=M):
-            _, wq, sp, _ = layers[0]
-            for l in range(LAYERS):
-                gemm(M, l, wq, sp)
-        t = time_graph(torch, hot_m, 300, 10) / LAYERS
-        hot_l2[str(M)] = {"us_per_launch": t * 1e6, "alg_gbs": alg_bytes(M, N_, K_, G_, False) / t / 1e9}
-
     # ---- end to end through the C ABI: host activations in, host outputs out ----
-    A_pin = {M: A_host[M].pin_memory() for M in MS}
+    A_pin = {M: A_host[:M].clone().pin_memory() for M in MS}
     C_pin = {M: torch.empty(LAYERS, M, N_, dtype=tdt).pin_memory() for M in MS}
     h2d = sum(A_pin[M].numel() * 2 for M in MS)
     d2h = sum(C_pin[M].numel() * 2 for M in MS)
     e2e_steps = max(1, min(args.steps, 300))
+    A_in = {M: torch.empty(M, K_, dtype=tdt, device="cuda") for M in MS}
 
     def e2e_step():
         for M in MS:
-            A_dev[M].copy_(A_pin[M], non_blocking=True)
+            A_in[M].copy_(A_pin[M], non_blocking=True)
             for l, (_, wq, sp, _) in enumerate(layers):
-                gemm(M, l, wq, sp)
+                B.gemm_ex(A_in[M], wq, sp, None, None, C_view[M][l], M, N_, K_, G_, QTYPE, DTYPE, "auto",
+                          static_weights=True)
             C_pin[M].copy_(C_dev[M], non_blocking=True)
     for _ in range(3):
         e2e_step()
@@ -606,29 +643,33 @@ def main():
 
     extra = {}
     if rank == 0 and not args.no_extras:
+        del C_big
+        torch.cuda.empty_cache()
         extra = extras(torch, B, synth, peaks)
 
-    # roofline of the dominant kernel (the decode kernel: every launch in the step)
+    # roofline of the dominant kernel (the small-M kernel: every launch in the step)
     t_launch = t_dev / (args.steps * launches_per_step)
     achieved = (abytes_step / launches_per_step) / t_launch / 1e9
-    traffic = profiled_traffic("decode_kernel_m1_4_8_k4096_n4096.md",
+    traffic = profiled_traffic("decode_kernel_m1_k8192_n28672.md",
                                ["decode_kernel.cuh", "decode.cu", "common.cuh"], 1)
 
     cpu = None
     if rank == 0:
         import oracle as orc
         orc.build()
-        # bounded sample: the oracle on whole layers (cycling over the first four
-        # of the workload) until about 10 s of CPU time
-        tt, bb, nl = 0.0, 0, 0
-        while tt < 10.0 and nl < 400:
-            t, b = oracle_sample(N_, layer=nl % 4)
+        # bounded sample: the oracle on the first output columns of the layer for
+        # every decode M of the step, until about 10 s of CPU time
+        tt, bb, ns = 0.0, 0, 0
+        while tt < 10.0 and ns < 200:
+            t, b = oracle_sample(512, layer=ns % 2)
             tt += t
             bb += b
-            nl += 1
+            ns += 1
         cpu = {"value": bb / tt / 1e9, "unit": "GB/s", "cores": orc.num_threads(), "kind": "oracle",
-               "sample": f"{nl} whole-layer passes over 4 layers of the workload, M = 1, 4, 8 each "
-                         f"(unpack -> dequant -> float64 GEMM), {tt:.1f} s of CPU time"}
+               "cpu_model": cpu_model(),
+               "sample": f"{ns} passes over output columns 0..511 of the layer (2 weight copies), "
+                         f"M = {', '.join(map(str, MS))} each (unpack -> dequant -> float64 GEMM), "
+                         f"{tt:.1f} s of CPU time"}
 
     if rank == 0:
         line = {
@@ -637,21 +678,24 @@ def main():
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded SplitMix64 weights and activations)",
             "config": {"workload": WORKLOAD, "M": list(MS), "K": K_, "N": N_, "group_size": G_,
-                       "qtype": QTYPE, "act_dtype": DTYPE, "layers_per_step": LAYERS,
+                       "qtype": QTYPE, "act_dtype": DTYPE, "weight_copies": LAYERS,
                        "l2": f"inputs larger than L2: {LAYERS} distinct weight copies, "
                              f"{LAYERS * weight_bytes(N_, K_, G_, False) / 1e6:.0f} MB per pass",
                        "timing": "CUDA graph of one step replayed K times, CUDA events",
                        "call": "w4a16_gemm_ex(path=auto | W4A16_OPT_STATIC_WEIGHTS)",
+                       "per_m": "the same layer at every M of the crossover sweep, graph of both copies",
                        "parallelism": f"replicas x{world}"},
             "tflops": world * args.steps * flops_step / t_max / 1e12,
             "alg_gbs": world * args.steps * abytes_step / t_max / 1e9,
             "per_m": per_m,
             "step_spread": step_spread,
-            "hot_l2": hot_l2,
             "gpu_launches": args.steps * launches_per_step,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                          "frac": achieved / hbm_peak, "traffic": traffic,
                          "peak_kind": peak_kind, "kernel": "decode_kernel"},
+            "roofline_prefill": {"bound": "tensor", "achieved": per_m["4096"]["tflops"], "peak": tc_peak,
+                                 "unit": "TFLOP/s", "frac": per_m["4096"]["frac_of_bf16"],
+                                 "peak_kind": peak_kind, "kernel": per_m["4096"]["path"], "M": 4096},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps},
