@@ -83,8 +83,8 @@ def _configure(lib):
         "orc_unpack_q": (None, [P, I64, I64, I64, P]),
         "orc_zero_point": (I, [P, I64, I64, I64]),
         "orc_dequant": (None, [P, P, P, I64, I64, I64, I, P]),
-        "orc_gemm": (None, [P, P, I64, I64, I64, I, P]),
-        "orc_gemm_rows": (None, [P, P, P, I64, I64, I64, I, P]),
+        "orc_gemm": (I, [P, P, I64, I64, I64, I, P]),
+        "orc_gemm_rows": (I, [P, P, P, I64, I64, I64, I, P]),
         "orc_gemm_pairs": (None, [P, P, P, P, I64, I64, I, P]),
         "orc_linear_rows": (I, [P, P, I64, P, P, P, I64, I64, I64, I64, I, P]),
         "orc_add_bias": (None, [P, I64, I64, P, I]),
@@ -235,7 +235,8 @@ def gemm(A, W, dtype: str) -> np.ndarray:
     M, K = a.shape
     N = w.shape[0]
     out = np.empty((M, N), dtype=np.float64)
-    _load().orc_gemm(_ptr(a), _ptr(w), M, N, K, DTYPE_CODE[dtype], _ptr(out))
+    if _load().orc_gemm(_ptr(a), _ptr(w), M, N, K, DTYPE_CODE[dtype], _ptr(out)):
+        raise MemoryError("oracle: out of host memory")
     return out
 
 
@@ -246,7 +247,8 @@ def gemm_rows(A, W, rows, dtype: str) -> np.ndarray:
     K = a.shape[1]
     N = w.shape[0]
     out = np.empty((r.size, N), dtype=np.float64)
-    _load().orc_gemm_rows(_ptr(a), _ptr(w), _ptr(r), r.size, N, K, DTYPE_CODE[dtype], _ptr(out))
+    if _load().orc_gemm_rows(_ptr(a), _ptr(w), _ptr(r), r.size, N, K, DTYPE_CODE[dtype], _ptr(out)):
+        raise MemoryError("oracle: out of host memory")
     return out
 
 

@@ -245,32 +245,42 @@ static double dot_values(const double* a, const double* w, int64_t K) {
 /* Selected rows of C: out[i][n] = C[rows[i]][n] = sum_k A[rows[i]][k] W[n][k].
  * Each operand row is decoded to exact float64 values once; the sum runs over
  * k in increasing order. */
-void orc_gemm_rows(const uint16_t* A, const uint16_t* W, const int64_t* rows, int64_t nrows,
-                   int64_t N, int64_t K, int dtype, double* out) {
-    double* a = (double*)malloc((size_t)(nrows * K) * sizeof(double));
-    if (!a) return;
+/* Returns 0, or 1 when host memory for the float64 copies could not be had
+ * (the output is then incomplete and must not be used). */
+int orc_gemm_rows(const uint16_t* A, const uint16_t* W, const int64_t* rows, int64_t nrows,
+                  int64_t N, int64_t K, int dtype, double* out) {
+    double* a = (double*)malloc((size_t)(nrows * K > 0 ? nrows * K : 1) * sizeof(double));
+    if (!a) return 1;
+    int failed = 0;
     for (int64_t i = 0; i < nrows; ++i)
         for (int64_t k = 0; k < K; ++k) a[i * K + k] = dt_value(A[rows[i] * K + k], dtype);
 #pragma omp parallel
     {
-        double* w = (double*)malloc((size_t)K * sizeof(double));
+        double* w = (double*)malloc((size_t)(K > 0 ? K : 1) * sizeof(double));
+        if (!w) {
+#pragma omp atomic write
+            failed = 1;
+        }
 #pragma omp for schedule(static)
         for (int64_t n = 0; n < N; ++n) {
+            if (!w) continue;
             for (int64_t k = 0; k < K; ++k) w[k] = dt_value(W[n * K + k], dtype);
             for (int64_t i = 0; i < nrows; ++i) out[i * N + n] = dot_values(a + i * K, w, K);
         }
         free(w);
     }
     free(a);
+    return failed;
 }
 
-void orc_gemm(const uint16_t* A, const uint16_t* W, int64_t M, int64_t N, int64_t K,
-              int dtype, double* C) {
+int orc_gemm(const uint16_t* A, const uint16_t* W, int64_t M, int64_t N, int64_t K,
+             int dtype, double* C) {
     int64_t* rows = (int64_t*)malloc((size_t)(M > 0 ? M : 1) * sizeof(int64_t));
-    if (!rows) return;
+    if (!rows) return 1;
     for (int64_t m = 0; m < M; ++m) rows[m] = m;
-    orc_gemm_rows(A, W, rows, M, N, K, dtype, C);
+    const int rc = orc_gemm_rows(A, W, rows, M, N, K, dtype, C);
     free(rows);
+    return rc;
 }
 
 /* Selected elements: out[i] = C[ms[i]][ns[i]]. */
@@ -303,8 +313,8 @@ int orc_linear_rows(const uint16_t* A, const uint32_t* words, int64_t ldq, const
     if (!q || !w) { free(q); free(w); return 1; }
     orc_unpack_q(words, N, K, ldq, q);
     orc_dequant(q, scales, zeros, N, K, G_eff, dtype, w);
-    orc_gemm_rows(A, w, rows, nrows, N, K, dtype, out);
+    const int rc = orc_gemm_rows(A, w, rows, nrows, N, K, dtype, out);
     free(q);
     free(w);
-    return 0;
+    return rc;
 }
