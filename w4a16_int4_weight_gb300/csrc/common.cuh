@@ -136,6 +136,34 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
     return mbar_wait_limit(bar, parity, status, site, kWaitLimitNs);
 }
 
+// The same wait with a long suspend-time hint on each try: a waiting thread
+// sleeps until the phase completes instead of re-polling, so waiting warps
+// leave their issue slots to the others (the limit stays bounded).
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, int* status, int site,
+                                                uint64_t limit_ns = kWaitLimitNs) {
+    const uint32_t a = smem_u32(bar);
+    auto try_wait = [&]() {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 2000000;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(a), "r"(parity)
+            : "memory");
+        return ok != 0;
+    };
+    if (try_wait()) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (!try_wait()) {
+        if (global_timer_ns() - t0 > limit_ns) {
+            atomicCAS(status, 0, site);
+            return false;
+        }
+    }
+    return true;
+}
+
 // ---------------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor), completion through an mbarrier transaction count
 // ---------------------------------------------------------------------------

@@ -203,6 +203,9 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
             for (int i = max(0, issued - p.stages); i < issued; ++i)
                 mbar_wait(&full[i % p.stages], uint32_t(i / p.stages) & 1u, p.status, 2);
         }
+        // The other lanes wait here for lane 0 (blocked, not polling the
+        // reduction barrier below for the whole K loop).
+        __syncwarp();
     } else {
         // ------------------------------ consumers -----------------------------
         float accg[NSETS][NT][4];
@@ -298,7 +301,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
         int stage = 0;
         uint32_t wrap = 0;   // pass over the ring, mod 2: the phase parity to wait for
         for (int i = 0; i < nb; ++i) {
-            const bool got = __all_sync(0xffffffffu, mbar_wait(&full[stage], wrap, p.status, 1));
+            const bool got = __all_sync(0xffffffffu, mbar_wait_sleep(&full[stage], wrap, p.status, 1));
             if (!got) { failed = true; break; }
             const StageView v = stage_view(smem, p, stage);
             const int box_k = (b_lo + i) * kBoxK;
@@ -374,7 +377,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
         }
     }
     // Once red_bar completes no peer writes here any more, so the CTA may retire.
-    const bool got = mbar_wait_limit(red_bar, 0u, p.status, 4, kReductionWaitLimitNs);
+    const bool got = mbar_wait_sleep(red_bar, 0u, p.status, 4, kReductionWaitLimitNs);
     const int any_failed = __syncthreads_or(failed || !got);
     const int items = rows_per * p.M;
     for (int it = tid; it < items; it += kThreads) {
