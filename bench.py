@@ -615,27 +615,54 @@ def main():
                    "p50_ms": step_ms[len(step_ms) // 2], "p90_ms": step_ms[(9 * len(step_ms)) // 10]}
 
     # ---- end to end through the C ABI: host activations in, host outputs out ----
+    # Each step copies every M's activations in from pinned host memory and every
+    # output back.  Input and output copies run on two more streams, ordered
+    # against the layer calls by events: an M's input copy waits until the
+    # previous step's calls of that M have finished reading the buffer, its
+    # calls wait for the input and for the previous step's output copy, and its
+    # output copy waits for its calls.  The copies of one M then overlap the
+    # other M's calls, as a serving loop overlaps them; every copy of the timed
+    # steps starts after the start event and ends before the stop event.
     A_pin = {M: A_host[:M].clone().pin_memory() for M in MS}
     C_pin = {M: torch.empty(LAYERS, M, N_, dtype=tdt).pin_memory() for M in MS}
     h2d = sum(A_pin[M].numel() * 2 for M in MS)
     d2h = sum(C_pin[M].numel() * 2 for M in MS)
     e2e_steps = max(1, min(args.steps, 300))
     A_in = {M: torch.empty(M, K_, dtype=tdt, device="cuda") for M in MS}
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = {M: torch.cuda.Event() for M in MS}      # input copied
+    ev_done = {M: torch.cuda.Event() for M in MS}    # the M's layer calls finished
+    ev_out = {M: torch.cuda.Event() for M in MS}     # output copied back
+    ev_start = torch.cuda.Event()
 
     def e2e_step():
         for M in MS:
-            A_in[M].copy_(A_pin[M], non_blocking=True)
+            s_in.wait_event(ev_done[M])
+            with torch.cuda.stream(s_in):
+                A_in[M].copy_(A_pin[M], non_blocking=True)
+            ev_in[M].record(s_in)
+            stream.wait_event(ev_in[M])
+            stream.wait_event(ev_out[M])
             for l, (_, wq, sp, _) in enumerate(layers):
                 B.gemm_ex(A_in[M], wq, sp, None, None, C_view[M][l], M, N_, K_, G_, QTYPE, DTYPE, "auto",
                           static_weights=True)
-            C_pin[M].copy_(C_dev[M], non_blocking=True)
+            ev_done[M].record(stream)
+            s_out.wait_event(ev_done[M])
+            with torch.cuda.stream(s_out):
+                C_pin[M].copy_(C_dev[M], non_blocking=True)
+            ev_out[M].record(s_out)
     for _ in range(3):
         e2e_step()
     torch.cuda.synchronize()
     barrier(world)
     e0.record(stream)
+    ev_start.record(stream)
+    s_in.wait_event(ev_start)
+    s_out.wait_event(ev_start)
     for _ in range(e2e_steps):
         e2e_step()
+    stream.wait_stream(s_out)   # the last outputs are back before the clock stops
+    stream.wait_stream(s_in)
     e1.record(stream)
     torch.cuda.synchronize()
     t_e2e = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
