@@ -76,8 +76,12 @@ constexpr int kTmemColsPerCta = 256;
 constexpr int kTmemStagesPerCta = 4;
 
 // Ring depths per token tile (16, 32, 64 or 128 tokens): two CTAs per SM (one
-// with the split-K buffer at BT >= 64), 96-128 KB of packed weights in flight
-// per SM.
+// with the split-K buffer at BT >= 64), 64-128 KB of packed weights in flight
+// per SM.  From 32 to 64 tokens, three weight stages and three or four activation
+// units: with two units the activation copy for unit u + 2 was requested only
+// when the dequantisers started unit u, and dequantiser warp 0 waited for it
+// (70B MLP, 32 / 64 tokens: 50.4 -> 48.5 / 51.4 -> 49.5 us; 14336 x 4096 at
+// 64 tokens: 19.3 -> 18.9 us).
 template <int BT>
 struct Layout {
     static_assert(BT == 16 || BT == 32 || BT == 64 || BT == 128, "token tile");
@@ -87,8 +91,8 @@ struct Layout {
     // one-block units at every token tile, most at 128 tokens: 66 -> 58 us on
     // the 70B MLP).
     static constexpr int kUnit = 2;
-    static constexpr int kWStages = BT <= 32 ? 4 : BT <= 64 ? 3 : 2;
-    static constexpr int kAUnits = BT <= 16 ? 4 : 2;                  // activation unit-slots
+    static constexpr int kWStages = BT <= 16 ? 4 : BT <= 64 ? 3 : 2;
+    static constexpr int kAUnits = BT <= 32 ? 4 : BT <= 64 ? 3 : 2;   // activation unit-slots
     static constexpr int kTmemCols = kTmemColsPerCta;
     static constexpr int kTmemStages = kTmemStagesPerCta;             // 32-column block stages
     static constexpr int kTUnits = kTmemStages / kUnit;               // tensor-memory unit-slots
@@ -285,8 +289,11 @@ __global__ void __launch_bounds__(kThreads, 2) tmem_gemm_kernel(const __grid_con
             for (int u = 0; u < nunits && good; ++u) {
                 const int s = u % kAUnits, tu = u % kTUnits;
                 // dq_full completes only after dequant warp 0 has seen the unit's
-                // activation tiles land (a_full), so one wait covers both
-                good = mbar_wait(&dq_full[tu], uint32_t(u / kTUnits) & 1u, p.status, 35);
+                // activation tiles land (a_full), so one wait covers both.  The
+                // issuer sleeps in it rather than polling, which leaves its
+                // scheduler's issue slots to the dequantisers there (1-5 % at
+                // 24-128 tokens).
+                good = mbar_wait_sleep(&dq_full[tu], uint32_t(u / kTUnits) & 1u, p.status, 35);
                 if (!good) break;
                 tc_fence_after();
                 const int nb = min(kUnit, nkb - kUnit * u);
