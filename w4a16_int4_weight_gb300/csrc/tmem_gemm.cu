@@ -45,7 +45,7 @@ cudaError_t launch_t(const CUtensorMap* maps, const tgemm::Params& p, int grid_x
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid_x, grid_y);
-    cfg.blockDim = dim3(tgemm::kThreads);
+    cfg.blockDim = dim3(tgemm::threads_for(BT));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
@@ -91,7 +91,7 @@ int resident_ctas(bool split) {
     const int smem = tmem_safe_smem(split ? L::kBytesRed : L::kBytesNoRed, L::kTmemCols);
     int by_smem = kSmemPerSm / (smem + kSmemPerCtaReserved);
     int by_tmem = 512 / L::kTmemCols;
-    int by_threads = 2048 / tgemm::kThreads;
+    int by_threads = 2048 / tgemm::threads_for(BT);
     return by_smem < by_tmem ? (by_smem < by_threads ? by_smem : by_threads)
                              : (by_tmem < by_threads ? by_tmem : by_threads);
 }
