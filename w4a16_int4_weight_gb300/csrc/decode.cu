@@ -59,7 +59,11 @@ int decode_scale_box_rows(int64_t g_eff, int64_t ng) {
 //   in flight weight bytes requested ahead per SM (up to 10% below 64 KB);
 //   room      small layers run best when the next kernel's CTAs fit beside
 //             this one's, so that their weight prefetch (PDL) overlaps it
-//             (60% when they do not fit, for <= 12 boxes per SM);
+//             (60% when they do not fit, for <= 12 boxes per SM); with
+//             32-wide groups (eight rescales per box) only when the SMs hold
+//             more than 2.5 CTAs on average (measured, M = 8 with zero points:
+//             11008 x 4096 four-way split 10.6 us against two-way 13.1 us,
+//             14336 x 4096 four-way 14.6 us against two-way 13.4 us);
 //   one CTA   a lone CTA per SM hides latency worse (20%);
 //   split     each doubling of ks costs 3% (reduction).
 bool plan_decode(int64_t M, int64_t N, int64_t K, int64_t g_eff, int64_t ng, bool zp,
@@ -69,7 +73,8 @@ bool plan_decode(int64_t M, int64_t N, int64_t K, int64_t g_eff, int64_t ng, boo
     const int nt = M <= 8 ? 1 : M <= 16 ? 2 : M <= 32 ? 4 : 8;
     const int64_t row_tiles = (N + kBN - 1) / kBN;
     const int64_t nboxes = (K + kBoxK - 1) / kBoxK;
-    const int sb = stage_bytes_for(M, decode_scale_box_rows(g_eff, ng), zp);
+    const int gps = decode_scale_box_rows(g_eff, ng);
+    const int sb = stage_bytes_for(M, gps, zp);
     const int max_ctas = nt == 1 ? 4 : nt == 2 ? 3 : 1;   // register limit of the instantiations
     constexpr int kMaxPlanStages = 5;                       // the range the model was fitted on
     double best_cost = 0.0;
@@ -93,7 +98,7 @@ bool plan_decode(int64_t M, int64_t N, int64_t K, int64_t g_eff, int64_t ng, boo
             const double work = double(per * bp);
             double cost = work * (1.0 + 0.2 * double(waves - 1));
             if (inflight_kb < 64.0) cost *= 1.0 + 0.1 * (64.0 - inflight_kb) / 64.0;
-            if (work <= 12.0 && r - per < per) cost *= 1.6;
+            if (work <= 12.0 && r - per < per && (gps < 8 || 2 * ctas > 5 * int64_t(num_sms))) cost *= 1.6;
             if (per == 1) cost *= 1.2;
             int lg = 0;
             for (int k = ks; k > 1; k >>= 1) ++lg;
