@@ -33,6 +33,8 @@ SHAPES = [
     (513, 1024, 2048, 32, "uint4", "bf16"),
     (129, 256, 1024, 256, "uint4", "fp16"),
     (12, 256, 1024, 32, "uint4", "bf16"),      # G = 32 between 9 and 16 tokens: routed to the fused kernel
+    (24, 136, 128, 32, "uint4", "bf16"),       # one MMA hand-off: the second issuer has none
+    (48, 200, 64, -1, "uint4b8", "fp16"),      # one 64-wide block
 ]
 
 
@@ -114,11 +116,13 @@ def test_one_hot_activations_return_dequantised_weights_exactly(path, dtype):
     assert np.array_equal(C, w_ref[:, km].T)
 
 
-@pytest.mark.parametrize("path", ["decode", "fused_tmem", "fused_smem", "dense"])
-def test_integer_valued_gemm_is_exact(path):
+@pytest.mark.parametrize("path,M", [("decode", 16), ("fused_tmem", 16), ("fused_tmem", 40), ("fused_smem", 16),
+                                    ("dense", 16)])
+def test_integer_valued_gemm_is_exact(path, M):
     # scale 1, A in {-1, 0, 1}: every partial sum is an integer below 2^24, so the
-    # fp32 accumulation is exact in any order and C = rne_dtype(exact).
-    M, N, K = 16, 192, 512
+    # fp32 accumulation is exact in any order (also split between the tensor-memory
+    # kernel's two accumulators at 40 tokens) and C = rne_dtype(exact).
+    N, K = 192, 512
     p = _problem(M, N, K, -1, "uint4b8", "bf16")
     rng = np.random.default_rng(5)
     q = rng.integers(0, 16, (N, K)).astype(np.uint8)
@@ -151,6 +155,20 @@ def test_every_decode_m_up_to_64():
     for M in range(1, 65):
         C = run_gemm(w, x.A[:M], path="decode")
         assert orc.rel_error(orc.values(C, "bf16"), C_ref[:M]) <= TOL["bf16"], M
+
+
+def test_every_fused_m_from_17_to_72():
+    # 32- and 64-token tiles with two MMA issuers, an odd number of hand-offs
+    # (17 blocks of 64) and the 128-token tile just above
+    N, K = 136, 1088
+    p = _problem(72, N, K, 64, "uint4", "bf16")
+    x = synth.make_inputs(p)
+    w = DeviceWeight(p, x.q, x.scales, x.zeros)
+    C_ref = orc.linear(x.A, x.q, x.scales, x.zeros, 64, "bf16")
+    for M in range(17, 73):
+        C = run_gemm(w, x.A[:M], path="fused_tmem")
+        assert orc.rel_error(orc.values(C, "bf16"), C_ref[:M]) <= TOL["bf16"], M
+    assert_device_status_ok()
 
 
 def test_outputs_outside_c_are_untouched():
