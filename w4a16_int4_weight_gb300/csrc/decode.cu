@@ -1,6 +1,7 @@
 // Host side of the small-M kernel: launch planning (cluster split of K, ring
 // depth, shared memory), dispatch to the per-dtype instantiations, and the
 // module's device status word.  The kernel itself is in decode_kernel.cuh.
+#include <algorithm>
 #include <mutex>
 
 #include "decode_kernel.cuh"
@@ -11,13 +12,21 @@ namespace {
 
 __device__ int g_status;
 
-// Activation box slot: M token rows of 256 values (512 bytes each), in 1024-byte
-// units so that the scales behind it stay 128-byte aligned for TMA.
-int a_slot_for(int64_t M) { return int((M * 512 + 1023) / 1024 * 1024); }
+// Token tiles of 8 of the kernel instantiation that serves M tokens.
+int nt_for(int64_t M) { return M <= 8 ? 1 : M <= 16 ? 2 : M <= 32 ? 4 : 8; }
 
-// Token columns of the split-K reduction buffer: M rounded up to even (partials
-// travel as pairs of token columns).
-int red_cols_for(int64_t M) { return int((M + 1) / 2 * 2); }
+// Activation box slot: one token tile: M rows of 256 values (512 bytes each), in
+// 1024-byte units so that the scales behind it stay 128-byte aligned for TMA;
+// more: four 64-value sub-boxes of the kernel's 8 NT rows x 128 bytes, each
+// 1024-byte aligned for the 128-byte swizzle.
+int a_slot_for(int64_t M) { return M <= 8 ? int((M * 512 + 1023) / 1024 * 1024) : 4096 * nt_for(M); }
+
+// Columns of the split-K reduction buffer: partials travel as pairs of MMA
+// columns.  One token tile: tokens 2t, 2t + 1, so M rounded up to even; more:
+// tokens 8j + t and 8j + t + 4 (t < 4), one pair for each t with 8j + t < M.
+int red_cols_for(int64_t M) {
+    return M <= 8 ? int((M + 1) / 2 * 2) : int(2 * (4 * (M / 8) + std::min<int64_t>(4, M % 8)));
+}
 
 int stage_bytes_for(int64_t M, int gps, bool zp) {
     using namespace decode;
@@ -70,7 +79,7 @@ bool plan_decode(int64_t M, int64_t N, int64_t K, int64_t g_eff, int64_t ng, boo
                  int num_sms, int* ks_out, int* stages_out, size_t* smem_out, int* nt_out) {
     using namespace decode;
     if (M < 1 || M > kDecodeMaxM || num_sms < 1) return false;
-    const int nt = M <= 8 ? 1 : M <= 16 ? 2 : M <= 32 ? 4 : 8;
+    const int nt = nt_for(M);
     const int64_t row_tiles = (N + kBN - 1) / kBN;
     const int64_t nboxes = (K + kBoxK - 1) / kBoxK;
     const int gps = decode_scale_box_rows(g_eff, ng);
@@ -152,6 +161,7 @@ cudaError_t launch_decode(const CUtensorMap* maps, void* C, const void* bias, co
     p.gps = decode_scale_box_rows(s.g_eff, s.ng);
     if (p.gps < 1 || p.gps > kMaxGps) return cudaErrorInvalidValue;   // never expected
     p.a_slot = a_slot_for(s.M);
+    if (nt >= 2 && p.a_slot < 4 * 1024 * nt) return cudaErrorInvalidValue;   // sub-boxes must fit (never expected)
     p.mpr = red_cols_for(s.M);
     p.stage_bytes = stage_bytes_for(s.M, p.gps, s.zp);
     p.red_off = stages * p.stage_bytes + kBarBytes;

@@ -62,8 +62,10 @@ struct Params {
     int ks;           // CTAs per cluster (K split)
     int stages;       // ring depth (<= kMaxStages)
     int gps;          // scale-tile rows per box
-    int a_slot;       // bytes of the activation box slot: [M rows][256 values], 1024-byte units
-    int mpr;          // token columns of the reduction buffer: M rounded up to even
+    int a_slot;       // bytes of the activation box slot: one token tile: [M rows][256
+                      // values] in 1024-byte units; more: four 64-value sub-boxes
+                      // [8 NT rows][128 B] (128-byte swizzle), 1024 NT bytes each
+    int mpr;          // columns of the reduction buffer: two per stored pair of MMA columns
     int stage_bytes;  // bytes per stage (multiple of 1024): weights, activations, gps scale
                       // rows of 256 bytes and, with zero points, gps rows of 64 bytes
     int red_off;      // byte offset of the cluster reduction buffer
@@ -72,7 +74,7 @@ struct Params {
 
 struct StageView {
     uint8_t* w;        // [128 rows][128 B], 128-byte swizzle
-    uint8_t* a;        // [8 * NT rows][512 B], row-major
+    uint8_t* a;        // activation slot (see Params::a_slot)
     uint16_t* sc;      // [gps][128]
     uint32_t* zp;      // [gps][16]
 };
@@ -96,9 +98,17 @@ __device__ __forceinline__ void load_weights(const StageView& v, const CUtensorM
     if constexpr (ZP) tma_load_2d(v.zp, tz, bar, n0 / 8, g0);
 }
 
+// Two token tiles or more: four [M][64] copies (128-byte swizzle) into the
+// sub-boxes; one tile: one [M][256] copy.
+template <int NT>
 __device__ __forceinline__ void load_acts(const StageView& v, const CUtensorMap* ta,
                                           uint64_t* bar, int box) {
-    tma_load_2d(v.a, ta, bar, box * kBoxK, 0);
+    if constexpr (NT >= 2) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) tma_load_2d(v.a + i * (1024 * NT), ta, bar, box * kBoxK + 64 * i, 0);
+    } else {
+        tma_load_2d(v.a, ta, bar, box * kBoxK, 0);
+    }
 }
 
 // WPG: 32-wide word steps per quantisation group (1, 2, 4 for G = 32, 64, 128);
@@ -110,6 +120,9 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
                                                           const __grid_constant__ CUtensorMap tmap_z,
                                                           const Params p) {
     constexpr int MP = 8 * NT;                      // padded token count of the MMA column tiles
+    // Two token tiles or more: activations in 128-byte-swizzled sub-boxes and MMA
+    // columns permuted (below); one tile: plain rows, column g = token g.
+    constexpr bool SWZ = NT >= 2;
     // Independent accumulator chains per token tile.  Two chains shorten the MMA
     // dependency chain but cost a merge per group; measured on GB300 (70B MLP and
     // 11008x4096 layers, M = 1 and 8), one chain is faster at 32-wide groups
@@ -184,7 +197,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
                     mbar_arrive_expect_tx(&full[i], stage_tx);
                     load_weights<ZP>(v, &tmap_q, &tmap_s, &tmap_z, &full[i], b_lo + i, n0, p.g_eff);
                 }
-                load_acts(v, &tmap_a, &full[i], b_lo + i);
+                load_acts<NT>(v, &tmap_a, &full[i], b_lo + i);
             }
             // the next kernel in the stream may start its own prologue now
             grid_launch_dependents();
@@ -196,7 +209,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
                 const StageView v = stage_view(smem, p, s);
                 mbar_arrive_expect_tx(&full[s], stage_tx);
                 load_weights<ZP>(v, &tmap_q, &tmap_s, &tmap_z, &full[s], b_lo + issued, n0, p.g_eff);
-                load_acts(v, &tmap_a, &full[s], b_lo + issued);
+                load_acts<NT>(v, &tmap_a, &full[s], b_lo + issued);
                 if (++s == p.stages) { s = 0; wrap ^= 1u; }
             }
             // copies still in flight must land before the CTA retires
@@ -250,13 +263,30 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
         // swizzle), at byte r0*128 + ((ws ^ g) << 4) + 4t = wofs ^ (ws << 4) with g in
         // bits 4-6 of wofs; row r1 = r0 + 8 is 1024 bytes further.
         const int wofs = r0 * 128 + (g << 4) + (t << 2);
-        // MMA column g of tile j is token 8j + g.  Columns past M only reach outputs
-        // that are never stored, so their lanes re-read token M - 1 (a broadcast,
-        // and no token check in the loop).
-        int aoff[NT];
+        // MMA column g of tile j is token 8j + g with one token tile.  With more, it is
+        // token 8j + col_tok, col_tok = (g >> 1) | ((g & 1) << 2): a quarter-warp
+        // (g = 2p, 2p + 1) then reads two tokens 4 apart, whose 16-byte chunks the
+        // 128-byte swizzle of the sub-boxes puts on different banks (tokens 1 apart
+        // share them; 2-5 % at 16 tokens, nothing at 8 or fewer, where plain rows keep
+        // the stage smaller).  Columns whose token is past M reach only outputs that
+        // are never stored: their lanes read sub-box rows the copy did not write, or
+        // token M - 1 (plain rows, a broadcast).
+        const int col_tok = SWZ ? (g >> 1) | ((g & 1) << 2) : g;
+        // activation offsets of tile j: plain rows, K-values 8t .. 8t+7 of step ws at
+        // ws * 64; sub-boxes, at (ws / 2) * 1024 NT for even / odd steps
+        int aoff[NT][2];
 #pragma unroll
-        for (int j = 0; j < NT; ++j)
-            aoff[j] = min(8 * j + g, p.M - 1) * (kBoxK * 2) + (t << 4);   // K-values 8t .. 8t+7 of the step
+        for (int j = 0; j < NT; ++j) {
+            if constexpr (SWZ) {
+                // chunk (ws % 2) * 4 + t of row tok sits at chunk ^ (tok % 8), tok % 8 = col_tok
+                const int tok = 8 * j + col_tok;
+                aoff[j][0] = tok * 128 + ((t ^ col_tok) << 4);
+                aoff[j][1] = tok * 128 + (((4 | t) ^ col_tok) << 4);
+            } else {
+                aoff[j][0] = min(8 * j + col_tok, p.M - 1) * (kBoxK * 2) + (t << 4);
+                aoff[j][1] = 0;
+            }
+        }
 
         // One K box; CHECK: the box may end early at k_hi (the last box of a K range).
         auto run_box = [&](const StageView& v, int box_k, auto check_tag) {
@@ -278,10 +308,11 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
                     const uint32_t a_s0[4] = {q0[0], q1[0], q0[1], q1[1]};
                     const uint32_t a_s1[4] = {q0[2], q1[2], q0[3], q1[3]};
                     // activation K-values kw + 8t .. +7 of each token row
-                    const uint8_t* abox = v.a + ws * 64;
 #pragma unroll
                     for (int j = 0; j < NT; ++j) {
-                        const uint4 b = *reinterpret_cast<const uint4*>(abox + aoff[j]);
+                        const uint8_t* ap = SWZ ? v.a + (ws >> 1) * (1024 * NT) + aoff[j][ws & 1]
+                                                : v.a + ws * 64 + aoff[j][0];
+                        const uint4 b = *reinterpret_cast<const uint4*>(ap);
                         // step st = 2w + s of the group goes to set st % NSETS; a set's
                         // first step in a group starts from zero (per-group modes)
                         if (WPG < 8 && w == 0) {
@@ -330,7 +361,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
         }
     }
 
-    // C fragment: (row g, tokens 2t, 2t+1) and (row g + 8, same tokens)
+    // C fragment: (row g, columns 2t, 2t+1) and (row g + 8, same columns); column
+    // 2t + e of tile j is token 8j + 2t + e (one token tile) or 8j + t + 4e (more)
     const bool consumer = warp < kConsumerWarps;
     // the bias of an output row, 0 without one
     auto bias_of = [&](int n) { return p.bias && n < p.N ? to_f32<BF16>(p.bias[n]) : 0.f; };
@@ -343,7 +375,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
             for (int j = 0; j < NT; ++j) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const int tok = 8 * j + 2 * t + (e & 1);
+                    const int tok = SWZ ? 8 * j + t + 4 * (e & 1) : 8 * j + 2 * t + (e & 1);
                     const int n = n0 + (e < 2 ? r0 : r1);
                     if (tok < p.M && n < p.N)
                         p.C[size_t(tok) * p.ldc + n] =
@@ -365,12 +397,14 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {   // (row, tokens 2t and 2t+1) as one 8-byte store
-                const int tok = 8 * j + 2 * t;
-                if (tok >= p.M) continue;   // columns past M are never summed
+            for (int h = 0; h < 2; ++h) {   // (row, columns 2t and 2t+1) as one 8-byte store
+                // the pair holds tokens 8j + 2t, + 1 (one token tile) or 8j + t, + 4;
+                // pairs whose first token is past M are never summed
+                if ((SWZ ? 8 * j + t : 8 * j + 2 * t) >= p.M) continue;
+                const int col = 8 * j + 2 * t;
                 const int row = h == 0 ? r0 : r1;
                 const int owner = row / rows_per;
-                const uint32_t off = uint32_t(((rank * rows_per + (row - owner * rows_per)) * p.mpr + tok) * 4);
+                const uint32_t off = uint32_t(((rank * rows_per + (row - owner * rows_per)) * p.mpr + col) * 4);
                 st_async_f32x2(cluster_map(red_s + off, uint32_t(owner)), acc[j][2 * h], acc[j][2 * h + 1],
                                cluster_map(bar_s, uint32_t(owner)));
             }
@@ -382,8 +416,9 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     const int items = rows_per * p.M;
     for (int it = tid; it < items; it += kThreads) {
         const int rl = it % rows_per, tok = it / rows_per;
+        const int col = SWZ ? 8 * (tok >> 3) + 2 * (tok & 3) + ((tok >> 2) & 1) : tok;   // its reduction column
         float sum = 0.f;
-        for (int c = 0; c < p.ks; ++c) sum += red[(c * rows_per + rl) * p.mpr + tok];
+        for (int c = 0; c < p.ks; ++c) sum += red[(c * rows_per + rl) * p.mpr + col];
         const int n = n0 + rank * rows_per + rl;
         if (n < p.N) p.C[size_t(tok) * p.ldc + n] = any_failed ? nan_out : from_f32<BF16>(sum + bias_of(n));
     }

@@ -53,7 +53,7 @@ cudaError_t launch_dequant(const uint32_t* Wq, const void* scales, const int32_t
 
 // decode.cu: small-M split-K kernel, M <= kDecodeMaxM.
 constexpr int64_t kDecodeMaxM = 64;
-// maps: packed q [N][ldq] u32 box {32,128} SW128; A [M][K] box {256,M};
+// maps: packed q [N][ldq] u32 box {32,128} SW128; A [M][K] box {256,M} (M <= 8) or {64,M} SW128;
 // scales [ng][lds] box {128, decode_scale_box_rows}; zeros [ng][ldz] box {16, same}.
 // prefetch_weights: the weights are not written by work still running on the
 // stream, so they may be fetched before the previous grid completes.

@@ -351,8 +351,12 @@ w4a16_status launch_decode_path(const void* A, const void* Wq, const void* scale
     st = make_map(&maps[0], Wq, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, uint64_t(s.ldq), uint64_t(s.N),
                   uint64_t(s.ldq) * 4, 32, 128, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st) return st;
-    st = make_map(&maps[1], A, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, uint64_t(s.K), uint64_t(s.M),
-                  uint64_t(s.lda) * 2, 256, uint32_t(s.M), CU_TENSOR_MAP_SWIZZLE_NONE);
+    // one token tile (M <= 8): [M][256] boxes; more: [M][64] boxes with the 128-byte
+    // swizzle, four per K box (the small-M kernel's activation sub-boxes)
+    st = s.M <= 8 ? make_map(&maps[1], A, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, uint64_t(s.K), uint64_t(s.M),
+                             uint64_t(s.lda) * 2, 256, uint32_t(s.M), CU_TENSOR_MAP_SWIZZLE_NONE)
+                  : make_map(&maps[1], A, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, uint64_t(s.K), uint64_t(s.M),
+                             uint64_t(s.lda) * 2, 64, uint32_t(s.M), CU_TENSOR_MAP_SWIZZLE_128B);
     if (st) return st;
     st = make_map(&maps[2], scales, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, uint64_t(s.lds), uint64_t(s.ng),
                   uint64_t(s.lds) * 2, 128, gps, CU_TENSOR_MAP_SWIZZLE_NONE);
