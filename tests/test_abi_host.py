@@ -107,7 +107,9 @@ def test_router(B):
     assert B.route(1, 4096, 4096, 128, "uint4b8", "bf16") == B.PATH_DECODE
     assert B.route(16, 11008, 4096, 64, "uint4", "bf16") == B.PATH_DECODE
     assert B.route(8, 11008, 4096, 32, "uint4", "bf16") == B.PATH_DECODE
-    assert B.route(9, 11008, 4096, 32, "uint4", "bf16") == B.PATH_FUSED_TMEM   # G = 32 from 9 tokens
+    assert B.route(9, 11008, 4096, 32, "uint4", "bf16") == B.PATH_FUSED_TMEM   # G = 32 from 9 tokens, zero points
+    assert B.route(9, 11008, 4096, 32, "uint4b8", "bf16") == B.PATH_DECODE     # ... but not without them
+    assert B.route(16, 28672, 8192, 32, "uint4", "bf16") == B.PATH_DECODE      # ... nor on large layers
     assert B.route(16, 4096, 4096, -1, "uint4b8", "bf16") == B.PATH_DECODE     # one group
     assert B.route(17, 28672, 8192, 64, "uint4b8", "fp16") == B.PATH_FUSED_TMEM
     assert B.route(128, 28672, 8192, 64, "uint4", "bf16") == B.PATH_FUSED_TMEM

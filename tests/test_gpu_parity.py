@@ -32,7 +32,8 @@ SHAPES = [
     (40, 136, 4112, -1, "uint4b8", "bf16"),
     (513, 1024, 2048, 32, "uint4", "bf16"),
     (129, 256, 1024, 256, "uint4", "fp16"),
-    (12, 256, 1024, 32, "uint4", "bf16"),      # G = 32 between 9 and 16 tokens: routed to the fused kernel
+    (12, 256, 1024, 32, "uint4", "bf16"),      # G = 32 between 9 and 16 tokens with zero points: fused kernel
+    (13, 264, 2048, 32, "uint4b8", "bf16"),    # ... without them: small-M kernel, two token tiles
     (24, 136, 128, 32, "uint4", "bf16"),       # one MMA hand-off: the second issuer has none
     (48, 200, 64, -1, "uint4b8", "fp16"),      # one 64-wide block
 ]

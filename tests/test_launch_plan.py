@@ -72,8 +72,9 @@ def test_plans_keep_the_kernel_constraints(B):
             routed = B.lib.w4a16_route(M, N, K, G, B._qt(qt), B._dt(dt), int(has_dense))
             assert auto["path"] == B.PATH_NAMES[routed]
             # the router's crossovers (measured): small M on the split-K kernel, except
-            # 9..16 tokens at 32-wide groups; the dense copy from 2048 tokens
-            g32 = G == 32 and K > 32
+            # 9..16 tokens at 32-wide groups with zero points below 2^27 weights; the
+            # dense copy from 2048 tokens
+            g32 = G == 32 and K > 32 and qt == "uint4" and N * K < 2 ** 27
             if M <= 8 or (M <= 16 and not g32):
                 assert auto["path"] == "decode", (M, N, K, G)
             elif has_dense and M >= 2048:

@@ -230,11 +230,14 @@ int fused_kernel_for(int64_t) { return W4A16_PATH_FUSED_TMEM; }
 // the plan's K split and ring depth, chosen at launch from the live count.
 int route_impl(const LayerShape& s, bool has_dense) {
     const int64_t M = s.M;
-    // From 9 tokens (two MMA column tiles) the small-M kernel's per-group rescale
-    // at G = 32 costs more than the fused kernel's dequantisation (measured:
-    // 18.9 vs 15.5 us on 11008x4096; G >= 64 keeps decode ahead or level).
-    const bool small_groups = s.ng > 1 && s.g_eff <= 32;
-    if (M <= kDecodeUpToM && !(M > 8 && small_groups) && decode_plan_exists(M, s.N, s.K, s.g_eff, s.ng, s.zp))
+    // From 9 tokens (two MMA column tiles) at G = 32 with zero points, the small-M
+    // kernel's per-group rescale and zero-point reload cost more than the fused
+    // kernel's dequantisation except on large layers (measured, M = 9..16:
+    // 14336x4096 16.9-18.0 vs 15.4-15.5 us, 4096x4096 7.6-8.1 vs 6.9 us, but
+    // 28672x8192 46.4-47.1 vs 50.0 us; without zero points the small-M kernel is
+    // ahead or level on every layer measured, 28672x8192 38.6 vs 48.5 us).
+    const bool small_groups_zp = s.ng > 1 && s.g_eff <= 32 && s.zp && s.N * s.K < (int64_t(1) << 27);
+    if (M <= kDecodeUpToM && !(M > 8 && small_groups_zp) && decode_plan_exists(M, s.N, s.K, s.g_eff, s.ng, s.zp))
         return W4A16_PATH_DECODE;
     if (has_dense && M >= kDenseFromM) return W4A16_PATH_DENSE;
     return fused_kernel_for(M);
