@@ -172,6 +172,24 @@ def test_every_fused_m_from_17_to_72():
     assert_device_status_ok()
 
 
+def test_fused_whole_and_split_clusters():
+    # 224 row tiles of 32 tokens on the GPU's SMs: clusters of two that take two
+    # whole tiles next to clusters that split one tile's K (grid = 2 CTAs per SM)
+    N, K, G = 28672, 1024, 128
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    p = _problem(32, N, K, G, "uint4", "bf16")
+    x = synth.make_inputs(p)
+    w = DeviceWeight(p, x.q, x.scales, x.zeros)
+    C_ref = orc.linear(x.A, x.q, x.scales, x.zeros, G, "bf16")
+    for M in (17, 32):
+        plan = B().launch_plan(M, N, K, G, "uint4", "bf16", "fused_tmem", False, sms)
+        if sms < N // 128 < 2 * sms:
+            assert plan["k_split"] == 2 and plan["grid"] == 2 * sms
+        C = run_gemm(w, x.A[:M], path="fused_tmem")
+        assert orc.rel_error(orc.values(C, "bf16"), C_ref[:M]) <= TOL["bf16"], M
+    assert_device_status_ok()
+
+
 def test_outputs_outside_c_are_untouched():
     # C is written exactly over [M, N]: guard rows around it stay intact
     p = _problem(37, 200, 512, 64, "uint4", "fp16")

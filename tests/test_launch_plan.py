@@ -57,10 +57,17 @@ def check_tmem(p, M, N, K, sms):
     assert p["token_tile"] == tt
     ks = p["k_split"]
     assert ks in (1, 2, 4, 8)
+    tiles = cdiv(N, 128) * cdiv(M, tt)
     if ks > 1:
         assert cdiv(K, 256) // ks >= 2            # every CTA keeps at least two weight stages
         assert p["grid"] <= 2 * sms              # all CTAs of the split launch fit at once
-    assert p["grid"] == cdiv(N, 128) * cdiv(M, tt) * ks
+    if ks == 2 and p["grid"] != tiles * ks:
+        # between one and two 32-token tiles per SM: clusters of two take two whole
+        # tiles or split one, exactly two CTAs per SM
+        assert tt == 32 and sms < tiles < 2 * sms, (M, N, K, sms)
+        assert p["grid"] == 2 * sms
+    else:
+        assert p["grid"] == tiles * ks
     assert p["stages"] == 0 and p["smem_bytes"] == 0
 
 

@@ -80,6 +80,10 @@ cudaError_t launch_prefill(const CUtensorMap* maps, void* C, const void* bias, c
 int tmem_gemm_token_tile(int64_t M);
 // CTAs per cluster that split K (1, 2, 4 or 8) for the tensor-memory kernel.
 int tmem_gemm_ksplit(int64_t M, int64_t N, int64_t K, int num_sms);
+// The K split, the number of clusters that take whole tiles instead (see
+// tmem_gemm.cu), and the grid of a launch.
+void tmem_gemm_split(int64_t M, int64_t N, int64_t K, int num_sms, int* ks, int* whole_pairs);
+int64_t tmem_gemm_grid(int64_t M, int64_t N, int64_t K, int num_sms);
 cudaError_t launch_tmem_gemm(const CUtensorMap* maps, void* C, const void* bias, const LayerShape& s,
                              int num_sms, bool prefetch_weights, bool c_tma, cudaStream_t stream);
 int take_status_tmem_gemm();

@@ -120,15 +120,43 @@ bool split_fits(int bt) {
 // fit on the GPU at once (the split's reduction buffer lowers residency), so
 // that more dequantising warps share each SM.  Each CTA keeps >= 2 weight
 // stages (512 K-values).
-int tmem_gemm_ksplit(int64_t M, int64_t N, int64_t K, int num_sms) {
+//
+// Between one and two tiles per SM (32-token tiles, whose split buffer still
+// leaves two CTAs per SM) no split fits and whole tiles leave the SMs unevenly
+// loaded (70B MLP: 224 tiles, 72 SMs with two, 80 with one).  There clusters of
+// two either take two whole tiles or split one tile's K, so many of each that
+// the grid is exactly two CTAs per SM: whole_pairs = tiles - SMs, giving every
+// SM about 1.5 tiles of work instead of up to 2.
+void tmem_gemm_split(int64_t M, int64_t N, int64_t K, int num_sms, int* ks_out, int* whole_pairs_out) {
     const int bt = tmem_gemm_token_tile(M);
     const int64_t tiles = ((N + tgemm::kBM - 1) / tgemm::kBM) * ((M + bt - 1) / bt);
     const int64_t nws = (K + tgemm::kWK - 1) / tgemm::kWK;
-    if (!split_fits(bt)) return 1;
+    *ks_out = 1;
+    *whole_pairs_out = 0;
+    if (!split_fits(bt)) return;
     const int64_t cap = int64_t(resident_for(bt, true)) * num_sms;
     int ks = 1;
     while (ks < 8 && tiles * ks * 2 <= cap && nws / (2 * ks) >= 2) ks *= 2;
+    *ks_out = ks;
+    if (ks == 1 && bt == 32 && resident_for(bt, true) >= 2 && tiles > num_sms && tiles < 2 * int64_t(num_sms) &&
+        nws >= 4) {
+        *ks_out = 2;
+        *whole_pairs_out = int(tiles - num_sms);
+    }
+}
+
+int tmem_gemm_ksplit(int64_t M, int64_t N, int64_t K, int num_sms) {
+    int ks, wp;
+    tmem_gemm_split(M, N, K, num_sms, &ks, &wp);
     return ks;
+}
+
+int64_t tmem_gemm_grid(int64_t M, int64_t N, int64_t K, int num_sms) {
+    int ks, wp;
+    tmem_gemm_split(M, N, K, num_sms, &ks, &wp);
+    const int64_t tiles = ((N + tgemm::kBM - 1) / tgemm::kBM) * ((M + tmem_gemm_token_tile(M) - 1) / tmem_gemm_token_tile(M));
+    // whole_pairs clusters of ks CTAs hold ks tiles each, the rest one tile each
+    return int64_t(ks) * (wp + (tiles - int64_t(wp) * ks));
 }
 
 cudaError_t launch_tmem_gemm(const CUtensorMap* maps, void* C, const void* bias, const LayerShape& s,
@@ -147,11 +175,11 @@ cudaError_t launch_tmem_gemm(const CUtensorMap* maps, void* C, const void* bias,
     p.nkb = int((s.K + tgemm::kBK - 1) / tgemm::kBK);
     p.nws = int((s.K + tgemm::kWK - 1) / tgemm::kWK);
     p.gps = decode_scale_box_rows(p.g_eff, p.ng);
-    p.ks = tmem_gemm_ksplit(s.M, s.N, s.K, num_sms);
+    tmem_gemm_split(s.M, s.N, s.K, num_sms, &p.ks, &p.whole_pairs);
     p.prefetch_weights = prefetch_weights ? 1 : 0;
     p.c_tma = c_tma ? 1 : 0;
     const int bt = tmem_gemm_token_tile(s.M);
-    const int64_t ctas = ((s.N + tgemm::kBM - 1) / tgemm::kBM) * ((s.M + bt - 1) / bt) * p.ks;
+    const int64_t ctas = tmem_gemm_grid(s.M, s.N, s.K, num_sms);
     if (ctas > int64_t(0x7fffffff)) return cudaErrorInvalidValue;   // beyond any C that fits in memory
     const int gx = int(ctas);
     const int gy = 1;

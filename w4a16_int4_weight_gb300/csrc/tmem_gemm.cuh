@@ -71,6 +71,8 @@ struct Params {
     int nkb;           // ceil(K / kBK) MMA blocks
     int nws;           // ceil(K / kWK) weight stages
     int ks;            // CTAs per cluster (K split); 1 = whole K per CTA
+    int whole_pairs;   // with ks > 1: the first whole_pairs clusters take ks whole tiles
+                       // (one per CTA, no split), the others split one tile's K
     int prefetch_weights;
     int c_tma;         // tmap_c describes C (16-byte aligned base and row pitch): whole-K tiles
                        // leave through one TMA store of a shared-memory tile
@@ -197,17 +199,22 @@ __global__ void __launch_bounds__(threads_for(BT), 2) tmem_gemm_kernel(const __g
     float* red = reinterpret_cast<float*>(smem + L::kRedOff);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // blockIdx.x = (n tile * token tiles + token tile) * ks + rank: the ks CTAs of
-    // a cluster are consecutive, and token tiles vary fastest so that the CTAs
-    // sharing a weight tile run together and read it from L2 after the first
+    // blockIdx.x = cluster * ks + rank in the cluster: the ks CTAs of a cluster are
+    // consecutive.  Tile t = n tile * token tiles + token tile (token tiles vary
+    // fastest so that the CTAs sharing a weight tile run together and read it from
+    // L2 after the first).  Clusters below whole_pairs take ks whole tiles, one per
+    // CTA (ks tiles per cluster); the others split one tile's K ks ways.
     const int tiles_m = (p.M + BT - 1) / BT;
-    const int rank = p.ks > 1 ? int(blockIdx.x) % p.ks : 0;
-    const int tile = p.ks > 1 ? int(blockIdx.x) / p.ks : int(blockIdx.x);
+    const int cl = int(blockIdx.x) / p.ks, cr = int(blockIdx.x) % p.ks;
+    const bool whole = cl < p.whole_pairs;
+    const int ks = whole ? 1 : p.ks;              // this CTA's K split
+    const int rank = whole ? 0 : cr;
+    const int tile = whole ? cl * p.ks + cr : p.whole_pairs * p.ks + (cl - p.whole_pairs);
     const int n0 = (tile / tiles_m) * kBM;
     const int m0 = (tile % tiles_m) * BT;
     // this CTA's weight stages [ws_lo, ws_hi) and MMA blocks [kb_lo, kb_hi)
-    const int ws_lo = (rank * p.nws) / p.ks;
-    const int ws_hi = ((rank + 1) * p.nws) / p.ks;
+    const int ws_lo = (rank * p.nws) / ks;
+    const int ws_hi = ((rank + 1) * p.nws) / ks;
     const int nws = ws_hi - ws_lo;
     const int kb_lo = ws_lo * kSubPerW;
     const int kb_hi = min(ws_hi * kSubPerW, p.nkb);
@@ -238,9 +245,10 @@ __global__ void __launch_bounds__(threads_for(BT), 2) tmem_gemm_kernel(const __g
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (p.ks > 1) {
+    if (ks > 1) {
         // Peers store this CTA's rows of their partial tiles (kBM x BT fp32 in
         // all) only after the cluster barrier, i.e. after red_bar is initialised.
+        // (Clusters of whole tiles use neither the barrier nor red_bar.)
         if (tid == 0) mbar_arrive_expect_tx(red_bar, uint32_t(kBM * BT * 4));
         cluster_arrive_relaxed();
     }
@@ -489,7 +497,7 @@ __global__ void __launch_bounds__(threads_for(BT), 2) tmem_gemm_kernel(const __g
             if (tok < p.M) p.C[size_t(tok) * p.ldc + n] = nan_bits<BF16>();
         }
     };
-    if (p.ks == 1 && p.c_tma) {
+    if (ks == 1 && p.c_tma) {
         // Stage the output tile [BT tokens][128 rows] in the dtype in the activation
         // ring (the tensor core's last reads of it completed before acc_full), then
         // one TMA store; it clips rows >= N and tokens >= M.  Two-byte stores of
@@ -523,7 +531,7 @@ __global__ void __launch_bounds__(threads_for(BT), 2) tmem_gemm_kernel(const __g
         if (warp == kMmaWarp) tmem_dealloc(tmem, L::kTmemCols);
         return;
     }
-    if (p.ks == 1) {
+    if (ks == 1) {
         if (epi && !(ok && nkb > 0)) {
             nan_tile();
         } else if (epi) {
@@ -552,7 +560,7 @@ __global__ void __launch_bounds__(threads_for(BT), 2) tmem_gemm_kernel(const __g
     // rows only (a cluster-wide release barrier costs about a microsecond).  Every
     // row's columns are always sent, zeros after a failed wait, so that red_bar
     // completes.
-    const int rows_per = kBM / p.ks;
+    const int rows_per = kBM / ks;
     cluster_wait();   // every CTA's red_bar is initialised
     if (epi) {
         const int owner = row / rows_per;
@@ -579,7 +587,7 @@ __global__ void __launch_bounds__(threads_for(BT), 2) tmem_gemm_kernel(const __g
     for (int it = tid; it < items; it += threads_for(BT)) {
         const int rl = it % rows_per, col = it / rows_per;
         float sum = 0.f;
-        for (int c = 0; c < p.ks; ++c) sum += red[(size_t(c) * rows_per + rl) * BT + col];
+        for (int c = 0; c < ks; ++c) sum += red[(size_t(c) * rows_per + rl) * BT + col];
         const int n = n0 + rank * rows_per + rl, tok = m0 + col;
         if (n < p.N && tok < p.M)
             p.C[size_t(tok) * p.ldc + n] = any_failed ? nan_bits<BF16>() : from_f32<BF16>(sum + bias_of(n));

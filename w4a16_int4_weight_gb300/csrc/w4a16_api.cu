@@ -485,7 +485,7 @@ w4a16_status w4a16_launch_plan(int64_t M, int64_t N, int64_t K, int G, int qtype
         const int bt = tmem_gemm_token_tile(M);
         r.token_tile = bt;
         r.k_split = tmem_gemm_ksplit(M, N, K, num_sms);
-        r.grid = row_tiles * ((M + bt - 1) / bt) * r.k_split;
+        r.grid = tmem_gemm_grid(M, N, K, num_sms);
     } else if (path == W4A16_PATH_FUSED_SMEM) {
         const int bt = token_tile_for(M);
         r.token_tile = bt;
