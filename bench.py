@@ -67,8 +67,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true", help="skip the prefill/zero-point side measurements")
-    ap.add_argument("--profile-case", choices=["decode", "decode16", "decode_large", "decode_small", "zp", "mid", "prefill",
-                                               "prefill_smem", "dense", "dequant"],
+    ap.add_argument("--profile-case", choices=["decode", "decode16", "decode_large", "decode_small", "zp", "mid", "mid32",
+                                               "prefill", "prefill_smem", "dense", "dequant"],
                     help="only run `--reps` eager launches of one kernel (for ncu), then exit")
     ap.add_argument("--reps", type=int, default=8)
     ap.add_argument("--sweep", action="store_true",
@@ -412,13 +412,14 @@ def profile_case(args):
     from w4a16_int4_weight_gb300 import inputs as synth
     tdt = torch.bfloat16
     c = args.profile_case
-    if c in ("decode", "decode16", "decode_large", "decode_small", "zp", "mid"):
+    if c in ("decode", "decode16", "decode_large", "decode_small", "zp", "mid", "mid32"):
         M, N, K, G, qt = {"decode": (8, N_, K_, G_, QTYPE),
                           "decode16": (16, N_, K_, G_, QTYPE),
                           "decode_large": (1, 28672, 8192, 64, QTYPE),
                           "decode_small": (8, 4096, 4096, 128, QTYPE),
                           "zp": (16, 11008, 4096, 32, "uint4"),
-                          "mid": (64, 28672, 8192, 64, QTYPE)}[c]
+                          "mid": (64, 28672, 8192, 64, QTYPE),
+                          "mid32": (32, 28672, 8192, 64, QTYPE)}[c]
         lay = make_layers(torch, B, synth, 4, M, N, K, G, qt, "bf16")
         A = torch.randn(M, K, device="cuda").to(tdt)
         C = torch.empty(M, N, dtype=tdt, device="cuda")
