@@ -102,6 +102,22 @@ def test_plans_keep_the_kernel_constraints(B):
     assert n > 10000
 
 
+def test_fused_mixed_clusters_between_one_and_two_tiles_per_sm(B):
+    # 224 row tiles of 32 tokens: whole tiles would leave SMs unevenly loaded, so
+    # clusters of two take two whole tiles or split one, two CTAs on every SM
+    for sms in (148, 152, 200):
+        p = B.launch_plan(32, 28672, 8192, 64, "uint4b8", "bf16", "fused_tmem", False, sms)
+        assert (p["token_tile"], p["k_split"], p["grid"]) == (32, 2, 2 * sms)
+    # one tile per SM or fewer: the plain split; two or more: whole tiles
+    p = B.launch_plan(32, 28672, 8192, 64, "uint4b8", "bf16", "fused_tmem", False, 224)
+    assert (p["k_split"], p["grid"]) == (2, 448)
+    p = B.launch_plan(32, 28672, 8192, 64, "uint4b8", "bf16", "fused_tmem", False, 100)
+    assert (p["k_split"], p["grid"]) == (1, 224)
+    # 64-token tiles keep whole tiles (their split buffer leaves one CTA per SM)
+    p = B.launch_plan(64, 28672, 8192, 64, "uint4b8", "bf16", "fused_tmem", False, 152)
+    assert (p["k_split"], p["grid"]) == (1, 224)
+
+
 def test_route_does_not_depend_on_the_sm_count(B):
     # w4a16_route takes no SM count: the path AUTO resolves to must be the same
     # whatever SM count a launch is planned for, and the small-M plan must exist
