@@ -174,16 +174,18 @@ def test_every_fused_m_from_17_to_72():
 
 def test_fused_whole_and_split_clusters():
     # 224 row tiles of 32 tokens on the GPU's SMs: clusters of two that take two
-    # whole tiles next to clusters that split one tile's K (grid = 2 CTAs per SM)
+    # whole tiles next to clusters that split one tile's K (grid = 2 CTAs per SM).
+    # (64-token tiles do so from K = 8192, through the activation ring: covered on
+    # the full 70B layer by test_gpu_fullsize's sampled crossover test.)
     N, K, G = 28672, 1024, 128
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    p = _problem(32, N, K, G, "uint4", "bf16")
+    p = _problem(64, N, K, G, "uint4", "bf16")
     x = synth.make_inputs(p)
     w = DeviceWeight(p, x.q, x.scales, x.zeros)
     C_ref = orc.linear(x.A, x.q, x.scales, x.zeros, G, "bf16")
-    for M in (17, 32):
+    for M in (17, 32, 33, 64):
         plan = B().launch_plan(M, N, K, G, "uint4", "bf16", "fused_tmem", False, sms)
-        if sms < N // 128 < 2 * sms:
+        if M <= 32 and sms < N // 128 < 2 * sms:
             assert plan["k_split"] == 2 and plan["grid"] == 2 * sms
         C = run_gemm(w, x.A[:M], path="fused_tmem")
         assert orc.rel_error(orc.values(C, "bf16"), C_ref[:M]) <= TOL["bf16"], M

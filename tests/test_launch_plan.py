@@ -62,9 +62,9 @@ def check_tmem(p, M, N, K, sms):
         assert cdiv(K, 256) // ks >= 2            # every CTA keeps at least two weight stages
         assert p["grid"] <= 2 * sms              # all CTAs of the split launch fit at once
     if ks == 2 and p["grid"] != tiles * ks:
-        # between one and two 32-token tiles per SM: clusters of two take two whole
-        # tiles or split one, exactly two CTAs per SM
-        assert tt == 32 and sms < tiles < 2 * sms, (M, N, K, sms)
+        # between one and two 32- or 64-token tiles per SM: clusters of two take two
+        # whole tiles or split one, exactly two CTAs per SM
+        assert tt in (32, 64) and sms < tiles < 2 * sms, (M, N, K, sms)
         assert p["grid"] == 2 * sms
     else:
         assert p["grid"] == tiles * ks
@@ -113,8 +113,11 @@ def test_fused_mixed_clusters_between_one_and_two_tiles_per_sm(B):
     assert (p["k_split"], p["grid"]) == (2, 448)
     p = B.launch_plan(32, 28672, 8192, 64, "uint4b8", "bf16", "fused_tmem", False, 100)
     assert (p["k_split"], p["grid"]) == (1, 224)
-    # 64-token tiles keep whole tiles (their split buffer leaves one CTA per SM)
+    # the same at 64-token tiles (their split CTAs reduce through the activation ring)
     p = B.launch_plan(64, 28672, 8192, 64, "uint4b8", "bf16", "fused_tmem", False, 152)
+    assert (p["k_split"], p["grid"]) == (2, 304)
+    # 128-token tiles keep whole tiles
+    p = B.launch_plan(128, 28672, 8192, 64, "uint4b8", "bf16", "fused_tmem", False, 152)
     assert (p["k_split"], p["grid"]) == (1, 224)
 
 

@@ -48,6 +48,12 @@ __device__ __forceinline__ void cluster_arrive_relaxed() {
     asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
 }
 
+// Arrive with release semantics: this thread's earlier memory accesses (and what
+// it has observed) are ordered before the cluster peers' accesses after their wait.
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive;" ::: "memory");
+}
+
 __device__ __forceinline__ void cluster_wait() {
     asm volatile("barrier.cluster.wait;" ::: "memory");
 }

@@ -82,7 +82,7 @@ int tmem_gemm_token_tile(int64_t M);
 int tmem_gemm_ksplit(int64_t M, int64_t N, int64_t K, int num_sms);
 // The K split, the number of clusters that take whole tiles instead (see
 // tmem_gemm.cu), and the grid of a launch.
-void tmem_gemm_split(int64_t M, int64_t N, int64_t K, int num_sms, int* ks, int* whole_pairs);
+void tmem_gemm_split(int64_t M, int64_t N, int64_t K, int num_sms, int* ks, int* whole_pairs, int* red_in_ring);
 int64_t tmem_gemm_grid(int64_t M, int64_t N, int64_t K, int num_sms);
 cudaError_t launch_tmem_gemm(const CUtensorMap* maps, void* C, const void* bias, const LayerShape& s,
                              int num_sms, bool prefetch_weights, bool c_tma, cudaStream_t stream);

@@ -40,7 +40,7 @@ cudaError_t launch_t(const CUtensorMap* maps, const tgemm::Params& p, int grid_x
     // tcgen05.alloc blocks while the SM's 512 columns are taken; CTAs of one
     // cluster wait for each other, so more resident CTAs than 512 / kTmemCols
     // could deadlock.  Ask for enough shared memory that no more fit.
-    const int smem = tmem_safe_smem(p.ks > 1 ? L::kBytesRed : L::kBytesNoRed, L::kTmemCols);
+    const int smem = tmem_safe_smem(p.ks > 1 && !p.red_in_ring ? L::kBytesRed : L::kBytesNoRed, L::kTmemCols);
     cudaError_t e = ensure_smem(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -126,34 +126,47 @@ bool split_fits(int bt) {
 // loaded (70B MLP: 224 tiles, 72 SMs with two, 80 with one).  There clusters of
 // two either take two whole tiles or split one tile's K, so many of each that
 // the grid is exactly two CTAs per SM: whole_pairs = tiles - SMs, giving every
-// SM about 1.5 tiles of work instead of up to 2.
-void tmem_gemm_split(int64_t M, int64_t N, int64_t K, int num_sms, int* ks_out, int* whole_pairs_out) {
+// SM about 1.5 tiles of work instead of up to 2.  At 64-token tiles the split
+// buffer would leave one CTA per SM, so there the split CTAs reduce through the
+// activation ring instead, behind a cluster barrier after the K loop: worth it
+// from 32 weight stages (K >= 8192: 70B MLP 48.0 -> 46.2 us, 20480 x 8192
+// 46.5 -> 40.0 us), not at 16 (24576 x 4096: 25.0 -> 25.9 us).  The barrier
+// measured slower on every other split, and 128-token tiles slower too.
+void tmem_gemm_split(int64_t M, int64_t N, int64_t K, int num_sms, int* ks_out, int* whole_pairs_out,
+                     int* red_in_ring_out) {
     const int bt = tmem_gemm_token_tile(M);
     const int64_t tiles = ((N + tgemm::kBM - 1) / tgemm::kBM) * ((M + bt - 1) / bt);
     const int64_t nws = (K + tgemm::kWK - 1) / tgemm::kWK;
     *ks_out = 1;
     *whole_pairs_out = 0;
+    *red_in_ring_out = 0;
+    const bool mixed_range = tiles > num_sms && tiles < 2 * int64_t(num_sms) && nws >= 4;
+    if (bt == 64 && mixed_range && nws >= 32 && resident_for(bt, false) >= 2) {
+        *ks_out = 2;
+        *whole_pairs_out = int(tiles - num_sms);
+        *red_in_ring_out = 1;
+        return;
+    }
     if (!split_fits(bt)) return;
     const int64_t cap = int64_t(resident_for(bt, true)) * num_sms;
     int ks = 1;
     while (ks < 8 && tiles * ks * 2 <= cap && nws / (2 * ks) >= 2) ks *= 2;
     *ks_out = ks;
-    if (ks == 1 && bt == 32 && resident_for(bt, true) >= 2 && tiles > num_sms && tiles < 2 * int64_t(num_sms) &&
-        nws >= 4) {
+    if (ks == 1 && bt == 32 && resident_for(bt, true) >= 2 && mixed_range) {
         *ks_out = 2;
         *whole_pairs_out = int(tiles - num_sms);
     }
 }
 
 int tmem_gemm_ksplit(int64_t M, int64_t N, int64_t K, int num_sms) {
-    int ks, wp;
-    tmem_gemm_split(M, N, K, num_sms, &ks, &wp);
+    int ks, wp, ring;
+    tmem_gemm_split(M, N, K, num_sms, &ks, &wp, &ring);
     return ks;
 }
 
 int64_t tmem_gemm_grid(int64_t M, int64_t N, int64_t K, int num_sms) {
-    int ks, wp;
-    tmem_gemm_split(M, N, K, num_sms, &ks, &wp);
+    int ks, wp, ring;
+    tmem_gemm_split(M, N, K, num_sms, &ks, &wp, &ring);
     const int64_t tiles = ((N + tgemm::kBM - 1) / tgemm::kBM) * ((M + tmem_gemm_token_tile(M) - 1) / tmem_gemm_token_tile(M));
     // whole_pairs clusters of ks CTAs hold ks tiles each, the rest one tile each
     return int64_t(ks) * (wp + (tiles - int64_t(wp) * ks));
@@ -175,7 +188,7 @@ cudaError_t launch_tmem_gemm(const CUtensorMap* maps, void* C, const void* bias,
     p.nkb = int((s.K + tgemm::kBK - 1) / tgemm::kBK);
     p.nws = int((s.K + tgemm::kWK - 1) / tgemm::kWK);
     p.gps = decode_scale_box_rows(p.g_eff, p.ng);
-    tmem_gemm_split(s.M, s.N, s.K, num_sms, &p.ks, &p.whole_pairs);
+    tmem_gemm_split(s.M, s.N, s.K, num_sms, &p.ks, &p.whole_pairs, &p.red_in_ring);
     p.prefetch_weights = prefetch_weights ? 1 : 0;
     p.c_tma = c_tma ? 1 : 0;
     const int bt = tmem_gemm_token_tile(s.M);

@@ -73,6 +73,8 @@ struct Params {
     int ks;            // CTAs per cluster (K split); 1 = whole K per CTA
     int whole_pairs;   // with ks > 1: the first whole_pairs clusters take ks whole tiles
                        // (one per CTA, no split), the others split one tile's K
+    int red_in_ring;   // the split's reduction buffer is the activation ring (launched
+                       // without the buffer's own shared memory; see the epilogue)
     int prefetch_weights;
     int c_tma;         // tmap_c describes C (16-byte aligned base and row pitch): whole-K tiles
                        // leave through one TMA store of a shared-memory tile
@@ -196,7 +198,7 @@ __global__ void __launch_bounds__(threads_for(BT), 2) tmem_gemm_kernel(const __g
     uint64_t* acc_full = t_empty + kTUnits;
     uint64_t* red_bar = acc_full + 1;                                    // split K: partials pushed here
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red_bar + 1);
-    float* red = reinterpret_cast<float*>(smem + L::kRedOff);
+    float* red = reinterpret_cast<float*>(smem + (p.red_in_ring ? L::kActOff : L::kRedOff));
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // blockIdx.x = cluster * ks + rank in the cluster: the ks CTAs of a cluster are
@@ -250,7 +252,7 @@ __global__ void __launch_bounds__(threads_for(BT), 2) tmem_gemm_kernel(const __g
         // all) only after the cluster barrier, i.e. after red_bar is initialised.
         // (Clusters of whole tiles use neither the barrier nor red_bar.)
         if (tid == 0) mbar_arrive_expect_tx(red_bar, uint32_t(kBM * BT * 4));
-        cluster_arrive_relaxed();
+        if (!p.red_in_ring) cluster_arrive_relaxed();
     }
     const uint32_t tmem = *tmem_slot;
     const uint32_t tmem_d = tmem;                    // accumulator of issuer 0: columns [0, BT)
@@ -561,6 +563,15 @@ __global__ void __launch_bounds__(threads_for(BT), 2) tmem_gemm_kernel(const __g
     // row's columns are always sent, zeros after a failed wait, so that red_bar
     // completes.
     const int rows_per = kBM / ks;
+    if (p.red_in_ring) {
+        // The buffer is the activation ring: every thread here is past the
+        // dequantisers' wait for the accumulator (the MMAs, the ring's last
+        // readers, have completed; the producers' copies all landed) before the
+        // CTA arrives, and peers store into it only after all have arrived.
+        static_assert(L::kRedBytes <= L::kAUnits * L::kAUnitBytes, "the reduction buffer fits the activation ring");
+        __syncthreads();
+        cluster_arrive();
+    }
     cluster_wait();   // every CTA's red_bar is initialised
     if (epi) {
         const int owner = row / rows_per;
