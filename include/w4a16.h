@@ -245,7 +245,10 @@ int w4a16_route(int64_t M, int64_t N, int64_t K, int G, int qtype, int dtype, in
  *              CTA tile, the CTAs per cluster that split K (1 = none), the depth
  *              of the small-M kernel's TMA ring (0 for the other kernels), the
  *              CTAs launched and the small-M kernel's dynamic shared memory per
- *              CTA (0 for the other kernels).
+ *              CTA (0 for the other kernels).  For the tensor-memory kernel
+ *              between one and two tiles per SM, k_split 2 with a grid of two
+ *              CTAs per SM means clusters of two that take two whole tiles next
+ *              to clusters that split one tile's K.
  * Returns W4A16_ERR_INVALID_ARG for arguments w4a16_gemm_ex would reject
  * (pointers aside), W4A16_ERR_UNSUPPORTED where it would be unsupported.
  */
