@@ -63,3 +63,53 @@ def test_chained_layers_static_weights_graph_replay(M):
         err = orc.rel_error(orc.values(got, DT), ref)
         assert err <= TOL[DT], (l, err)
         a_bits = got             # the next layer's activations: this layer's output bits
+
+
+@pytest.mark.parametrize("M", [32, 64])
+def test_chained_layers_mixed_clusters_graph_replay(M):
+    # 20480 x 20480 layers: 160 row tiles, between one and two per SM, so the
+    # tensor-memory kernel runs clusters that take two whole tiles next to
+    # clusters that split one tile's K (at 64 tokens through the activation ring),
+    # chained and replayed from a graph like the 4096 x 4096 layers above
+    n = k = 20480
+    layers = 3
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    plan = B().launch_plan(M, n, k, G, QT, DT, "auto", False, sms)
+    assert plan["path"] == "fused_tmem"
+    if sms < n // 128 < 2 * sms:
+        assert (plan["k_split"], plan["grid"]) == (2, 2 * sms)
+    probs = [synth.Problem(M, n, k, G, QT, DT, seed=s) for s in range(layers)]
+    xs = [synth.make_weights(p) for p in probs]
+    ws = [DeviceWeight(p, q, s, z) for p, (q, s, z) in zip(probs, xs)]
+    a0_bits = synth.make_activations(synth.Problem(M, n, k, G, QT, DT, seed=7))
+    A0 = to_dev_bits(a0_bits, DT)
+    Cs = [torch.empty(M, n, dtype=torch.bfloat16, device="cuda") for _ in range(layers)]
+
+    def step():
+        a = A0
+        for w, C in zip(ws, Cs):
+            B().gemm_ex(a, w.Wq, w.scales, None, None, C, M, n, k, G, QT, DT, "auto", static_weights=True)
+            a = C
+
+    step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for _ in range(3):
+        for C in Cs:
+            C.fill_(float("nan"))
+        g.replay()
+    torch.cuda.synchronize()
+    assert_device_status_ok()
+
+    rows = np.array([0, M - 1])
+    a_bits = a0_bits[rows]
+    for l, ((q, s, _), C) in enumerate(zip(xs, Cs)):
+        got = to_host_bits(C)[rows]
+        ref = orc.linear(np.ascontiguousarray(a_bits), q, s, None, G, DT)
+        err = orc.rel_error(orc.values(got, DT), ref)
+        assert err <= TOL[DT], (l, err)
+        a_bits = got
+    del ws
+    torch.cuda.empty_cache()
