@@ -8,7 +8,9 @@ The layers are chained, as in a model: layer l + 1 reads layer l's output as its
 activations, and every output is reset to NaN before each replay, so an
 activation read that ran ahead of the previous kernel's completion would see NaN.
 Each layer is checked against the oracle on the GPU's own input bits (every
-token row, or 16 sampled rows at 2048 tokens).
+token row, or 16 sampled rows at 2048 tokens).  20480 x 20480 layers at 32 and
+64 tokens run the same way on the tensor-memory kernel's mixed whole/split
+cluster grids (2 sampled rows per layer).
 """
 
 import numpy as np
