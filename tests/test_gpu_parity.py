@@ -34,6 +34,7 @@ SHAPES = [
     (129, 256, 1024, 256, "uint4", "fp16"),
     (12, 256, 1024, 32, "uint4", "bf16"),      # G = 32 between 9 and 16 tokens with zero points: fused kernel
     (13, 264, 2048, 32, "uint4b8", "bf16"),    # ... without them: small-M kernel, two token tiles
+    (14, 200, 4112, -1, "uint4", "fp16"),      # two token tiles, a 16-value K tail in the last box
     (24, 136, 128, 32, "uint4", "bf16"),       # one MMA hand-off: the second issuer has none
     (48, 200, 64, -1, "uint4b8", "fp16"),      # one 64-wide block
 ]
