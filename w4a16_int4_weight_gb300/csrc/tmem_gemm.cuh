@@ -266,13 +266,23 @@ __global__ void __launch_bounds__(threads_for(BT), 2) tmem_gemm_kernel(const __g
             tma_prefetch_desc(&tmap_w);
             tma_prefetch_desc(&tmap_s);
             const uint32_t tx = kPkBytes + uint32_t(p.gps) * (kBM * 2 + (ZP ? (kBM / 8) * 4 : 0));
+            // With one token tile every weight byte is read once: evict-first L2
+            // policy.  With more, the token tiles of a row tile read it from L2.
+            const bool once = tiles_m == 1;
+            const uint64_t pol = l2_evict_first_policy();
             auto load_w = [&](int w) {
                 const int s = w % kWStages, ws = ws_lo + w;
                 const int g0 = (ws * kWK) / p.g_eff;   // first group of the stage
                 mbar_arrive_expect_tx(&w_full[s], tx);
-                tma_load_2d(pk_tile(s), &tmap_w, &w_full[s], ws * (kWK / 8), n0);
-                tma_load_2d(sc_tile(s), &tmap_s, &w_full[s], n0, g0);
-                if constexpr (ZP) tma_load_2d(zp_tile(s), &tmap_z, &w_full[s], n0 / 8, g0);
+                if (once) {
+                    tma_load_2d_hint(pk_tile(s), &tmap_w, &w_full[s], ws * (kWK / 8), n0, pol);
+                    tma_load_2d_hint(sc_tile(s), &tmap_s, &w_full[s], n0, g0, pol);
+                    if constexpr (ZP) tma_load_2d_hint(zp_tile(s), &tmap_z, &w_full[s], n0 / 8, g0, pol);
+                } else {
+                    tma_load_2d(pk_tile(s), &tmap_w, &w_full[s], ws * (kWK / 8), n0);
+                    tma_load_2d(sc_tile(s), &tmap_s, &w_full[s], n0, g0);
+                    if constexpr (ZP) tma_load_2d(zp_tile(s), &tmap_z, &w_full[s], n0 / 8, g0);
+                }
             };
             const int first = min(kWStages, nws);
             if (!p.prefetch_weights) grid_dependency_wait();
