@@ -48,6 +48,7 @@ PER_M = (1, 2, 4, 8, 16, 32, 64, 128, 256, 512, 1024, 4096)   # the "vs M" curve
 N_, K_, G_ = 28672, 8192, 64
 QTYPE, DTYPE = "uint4b8", "bf16"
 LAYERS = 2                                 # distinct weight copies: 2 x 125 MB > L2
+PER_M_PASSES = 4                           # passes over the copies in one "vs M" graph
 L2_BYTES = 129 * 1024 * 1024
 
 
@@ -328,8 +329,9 @@ def time_graph(torch, fn, reps, warmup):
 
 def extras(torch, B, synth, peaks):
     """Side measurements on the other workloads (not the headline): the decode
-    GEMV on the 7B attention shape, the prefill tcgen05 kernels (fused and
-    dense), the dequant kernel and the zero-point decode pair."""
+    GEMV on the 7B attention shape, the headline layer with fp16 activations,
+    the prefill tcgen05 kernels (fused and dense), the dequant kernel and the
+    zero-point decode pair."""
     hbm, tc_burst, _, kind = peaks
     out = {}
     tdt = torch.bfloat16
@@ -348,6 +350,26 @@ def extras(torch, B, synth, peaks):
         byts = alg_bytes(M, N, K, G, False)
         out[f"decode_m{M}_k4096_n4096_g128"] = {"us": t * 1e6, "gbs": byts / t / 1e9,
                                                "frac_of_hbm": byts / t / 1e9 / hbm}
+    del lay, Cs
+    torch.cuda.empty_cache()
+    # the 70B MLP layer with fp16 activations (K = 8192, N = 28672, G = 64,
+    # uint4b8), M = 1, 8, 16: two weight copies (250 MB > L2), each M a CUDA
+    # graph of PER_M_PASSES passes over both, as the "vs M" curve
+    N, K, G, L = 28672, 8192, 64, 2
+    hdt = torch.float16
+    lay = make_layers(torch, B, synth, L, 16, N, K, G, "uint4b8", "fp16", seed0=400)
+    A = torch.randn(16, K, device="cuda").to(hdt)
+    Cs = torch.empty(L, 16, N, dtype=hdt, device="cuda")
+    for M in (1, 8, 16):
+        def run_h(M=M):
+            for _ in range(PER_M_PASSES):
+                for l, (_, wq, sp, _) in enumerate(lay):
+                    B.gemm_ex(A, wq, sp, None, None, Cs[l], M, N, K, G, "uint4b8", "fp16", "auto",
+                              static_weights=True)
+        t = time_graph(torch, run_h, 75, 5) / (L * PER_M_PASSES)
+        byts = alg_bytes(M, N, K, G, False)
+        out[f"decode_fp16_m{M}_k8192_n28672_g64"] = {"us": t * 1e6, "gbs": byts / t / 1e9,
+                                                    "frac_of_hbm": byts / t / 1e9 / hbm}
     del lay, Cs
     torch.cuda.empty_cache()
     # prefill M=2048, K=4096, N=14336, G=128, uint4b8: 4 weight copies rotate
@@ -592,11 +614,17 @@ def main():
     names = {v: k for k, v in B.PATHS.items()}
     per_m = {}
     for M in PER_M:
-        def one_m(M=M):
-            for l, (_, wq, sp, _) in enumerate(layers):
-                gemm(M, l, wq, sp, C_big[l] if M not in C_view else None)
-        reps = 200 if M <= 64 else 30 if M <= 512 else 5
-        t = time_graph(torch, one_m, reps, 3) / LAYERS
+        # up to 128 tokens a graph replays PER_M_PASSES passes over both copies:
+        # a launch then follows another one as in the step (the first launch of
+        # a replay cannot overlap its predecessor); larger M one pass
+        passes = PER_M_PASSES if M <= 128 else 1
+
+        def one_m(M=M, passes=passes):
+            for _ in range(passes):
+                for l, (_, wq, sp, _) in enumerate(layers):
+                    gemm(M, l, wq, sp, C_big[l] if M not in C_view else None)
+        reps = 50 if M <= 64 else 30 if M <= 512 else 5
+        t = time_graph(torch, one_m, reps, 3) / (LAYERS * passes)
         ab = alg_bytes(M, N_, K_, G_, False)
         fl = 2.0 * M * N_ * K_
         t_star = max(ab / (hbm_peak * 1e9), fl / (tc_peak * 1e12))
@@ -714,7 +742,8 @@ def main():
                              f"{LAYERS * weight_bytes(N_, K_, G_, False) / 1e6:.0f} MB per pass",
                        "timing": "CUDA graph of one step replayed K times, CUDA events",
                        "call": "w4a16_gemm_ex(path=auto | W4A16_OPT_STATIC_WEIGHTS)",
-                       "per_m": "the same layer at every M of the crossover sweep, graph of both copies",
+                       "per_m": f"the same layer at every M of the crossover sweep: a CUDA graph of "
+                                f"{PER_M_PASSES} passes over both copies up to 128 tokens, one pass above",
                        "parallelism": f"replicas x{world}"},
             "tflops": world * args.steps * flops_step / t_max / 1e12,
             "alg_gbs": world * args.steps * abytes_step / t_max / 1e9,
