@@ -648,41 +648,50 @@ def main():
 
     # ---- end to end through the C ABI: host activations in, host outputs out ----
     # Each step copies every M's activations in from pinned host memory and every
-    # output back.  Input and output copies run on two more streams, ordered
-    # against the layer calls by events: an M's input copy waits until the
-    # previous step's calls of that M have finished reading the buffer, its
-    # calls wait for the input and for the previous step's output copy, and its
-    # output copy waits for its calls.  The copies of one M then overlap the
-    # other M's calls, as a serving loop overlaps them; every copy of the timed
-    # steps starts after the start event and ends before the stop event.
+    # output back.  Two sets of device activations and outputs alternate between
+    # steps; input and output copies run on two more streams, ordered against the
+    # layer calls by events: a step's input copies wait until the calls of the
+    # step before last (the set's last readers) have finished, its calls wait for
+    # its inputs and for that step's output copies, and its output copies wait
+    # for its calls.  A step's copies then overlap the neighbouring steps' calls,
+    # as a serving loop overlaps them, and the calls of one step follow each
+    # other with no wait between them; every copy of the timed steps starts
+    # after the start event and ends before the stop event.
     A_pin = {M: A_host[:M].clone().pin_memory() for M in MS}
     C_pin = {M: torch.empty(LAYERS, M, N_, dtype=tdt).pin_memory() for M in MS}
     h2d = sum(A_pin[M].numel() * 2 for M in MS)
     d2h = sum(C_pin[M].numel() * 2 for M in MS)
     e2e_steps = max(1, min(args.steps, 300))
-    A_in = {M: torch.empty(M, K_, dtype=tdt, device="cuda") for M in MS}
+    A_in = [{M: torch.empty(M, K_, dtype=tdt, device="cuda") for M in MS} for _ in range(2)]
+    C_set = [C_dev, {M: torch.empty(LAYERS, M, N_, dtype=tdt, device="cuda") for M in MS}]
+    C_set_view = [{M: [C_set[b][M][l] for l in range(LAYERS)] for M in MS} for b in range(2)]
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
-    ev_in = {M: torch.cuda.Event() for M in MS}      # input copied
-    ev_done = {M: torch.cuda.Event() for M in MS}    # the M's layer calls finished
-    ev_out = {M: torch.cuda.Event() for M in MS}     # output copied back
+    ev_in = [torch.cuda.Event() for _ in range(2)]      # a set's inputs copied
+    ev_done = [torch.cuda.Event() for _ in range(2)]    # a set's layer calls finished
+    ev_out = [torch.cuda.Event() for _ in range(2)]     # a set's outputs copied back
     ev_start = torch.cuda.Event()
+    cur = [0]
 
     def e2e_step():
+        b = cur[0]
+        cur[0] ^= 1
+        s_in.wait_event(ev_done[b])
+        with torch.cuda.stream(s_in):
+            for M in MS:
+                A_in[b][M].copy_(A_pin[M], non_blocking=True)
+        ev_in[b].record(s_in)
+        stream.wait_event(ev_in[b])
+        stream.wait_event(ev_out[b])
         for M in MS:
-            s_in.wait_event(ev_done[M])
-            with torch.cuda.stream(s_in):
-                A_in[M].copy_(A_pin[M], non_blocking=True)
-            ev_in[M].record(s_in)
-            stream.wait_event(ev_in[M])
-            stream.wait_event(ev_out[M])
             for l, (_, wq, sp, _) in enumerate(layers):
-                B.gemm_ex(A_in[M], wq, sp, None, None, C_view[M][l], M, N_, K_, G_, QTYPE, DTYPE, "auto",
-                          static_weights=True)
-            ev_done[M].record(stream)
-            s_out.wait_event(ev_done[M])
-            with torch.cuda.stream(s_out):
-                C_pin[M].copy_(C_dev[M], non_blocking=True)
-            ev_out[M].record(s_out)
+                B.gemm_ex(A_in[b][M], wq, sp, None, None, C_set_view[b][M][l], M, N_, K_, G_, QTYPE, DTYPE,
+                          "auto", static_weights=True)
+        ev_done[b].record(stream)
+        s_out.wait_event(ev_done[b])
+        with torch.cuda.stream(s_out):
+            for M in MS:
+                C_pin[M].copy_(C_set[b][M], non_blocking=True)
+        ev_out[b].record(s_out)
     for _ in range(3):
         e2e_step()
     torch.cuda.synchronize()
