@@ -439,3 +439,39 @@ def test_exllama_words_match_the_packed_section_without_padding():
     rng = np.random.default_rng(22)
     q = rng.integers(0, 16, (5, 40)).astype(np.uint8)    # K/8 = 5, ldq = 8
     assert np.array_equal(orc.encode_q(q, "exllama"), orc.pack_q(q, 8)[:, :5])
+
+
+# --------------------------------------------------------------------------
+# The parity metric: max|C - C_ref| / (max|C_ref| + 1e-6), the tolerance rule
+# every GPU parity test applies
+# --------------------------------------------------------------------------
+
+def test_rel_error_hand_cases():
+    # largest difference over the largest reference magnitude, not a mean or a per-element ratio
+    assert orc.rel_error(np.array([1.0, 2.0]), np.array([1.0, 4.0])) == pytest.approx(2.0 / (4.0 + 1e-6), rel=1e-12)
+    # signs: |(-3) - (-1)| = 2 over max|C_ref| = 1
+    assert orc.rel_error(np.array([-3.0, 0.0]), np.array([-1.0, 0.0])) == pytest.approx(2.0 / (1.0 + 1e-6), rel=1e-12)
+    # the worst element decides, wherever it sits in a 2-D result
+    C_ref = np.array([[10.0, -20.0], [5.0, 1.0]])
+    C = C_ref.copy()
+    C[1, 1] += 0.5
+    assert orc.rel_error(C, C_ref) == pytest.approx(0.5 / (20.0 + 1e-6), rel=1e-12)
+    # identical results and an all-zero reference
+    assert orc.rel_error(C_ref, C_ref) == 0.0
+    assert orc.rel_error(np.array([1e-7]), np.array([0.0])) == pytest.approx(1e-7 / 1e-6, rel=1e-12)
+
+
+def test_rel_error_reads_dtype_bits():
+    # bf16 0x3F80 = 1.0 and 0x4000 = 2.0; fp16 0x3C00 = 1.0 and 0x4000 = 2.0
+    got = np.array([0x3F80, 0x4000], dtype=np.uint16)
+    assert orc.rel_error(got, np.array([1.0, 2.5]), "bf16") == pytest.approx(0.5 / (2.5 + 1e-6), rel=1e-12)
+    got = np.array([0x3C00, 0x4000], dtype=np.uint16)
+    assert orc.rel_error(got, np.array([1.0, 2.0]), "fp16") == 0.0
+
+
+def test_rel_error_of_a_nan_output_fails_any_tolerance():
+    # a NaN canary left in an output must not pass "err <= tol"
+    err = orc.rel_error(np.array([1.0, np.nan]), np.array([1.0, 1.0]))
+    assert not (err <= 1e-2)
+    nan_bf16 = np.array([0x7FC0], dtype=np.uint16)
+    assert not (orc.rel_error(nan_bf16, np.array([1.0]), "bf16") <= 1e-2)
